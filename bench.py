@@ -1,0 +1,478 @@
+"""Benchmark: query-aware sparse paged decode steps on GB300.
+
+A step is one pass of the whole hot path over one batch: refresh the
+metadata of the page each sequence appends to, select the top-K pages per
+(sequence, KV head), and run sparse paged decode over them (three kernel
+launches).  Inputs are synthetic and resident in HBM (the KV pool exceeds
+the 129 MB L2, and the query rotates over 16 variants, so a step never finds
+its predecessor's selection in L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     # the CPU oracle on the host cores
+
+One JSON line on stdout (rank 0).  Under torchrun each rank decodes its own
+batch (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from query_aware_sparse_kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse paged decode: steps/s and effective HBM GB/s (% of GB300 peak)"
+DEFAULT_WORKLOAD = "llama3_8b"
+N_Q_VARIANTS = 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------ accounting --
+def _es(dtype) -> int:
+    return torch.tensor([], dtype=dtype).element_size()
+
+
+def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray | None) -> dict:
+    """Algorithmic bytes of one step, per kernel.
+
+    decode: K and V of every 16-token sub-tile holding a valid token of a
+            selected page (a whole page when P = 16), q, out, lse, the
+            selected list and one page-table entry per selected page;
+    select: the metadata (2 d values) of every page of every row, q, one
+            page-table entry per page, the fp32 score written and read back,
+            the selected list written;
+    meta:   the valid key rows of each sequence's last page, its 2 d values written.
+    """
+    spec = inputs["spec"]
+    B, Hq, Hkv, d, P = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
+    s = _es(spec.kv_dtype)
+    qs = _es(spec.q_dtype)
+    seq = inputs["seq_lens"].numpy().astype(np.int64)
+    nb = (seq + P - 1) // P
+    sub_bytes = 16 * d * s * 2  # K + V of one 16-token sub-tile
+    kv = 0
+    n_pages_read = 0
+    for b in range(B):
+        for g in range(Hkv):
+            if selected is None:
+                pages = range(int(nb[b]))
+            else:
+                pages = selected[b, g, :int(n_selected[b, g])]
+            for j in pages:
+                valid = min(P, int(seq[b]) - int(j) * P)
+                kv += ((valid + 15) // 16) * sub_bytes
+                n_pages_read += 1
+    q_bytes = B * Hq * d * qs
+    out_bytes = B * Hq * d * 4 + B * Hq * 4
+    top_k = spec.top_k
+    sel_bytes = 0 if top_k is None else B * Hkv * top_k * 4 + B * Hkv * 4
+    decode = kv + q_bytes + out_bytes + sel_bytes + n_pages_read * 4
+    if top_k is None:
+        select = 0
+    else:
+        total_pages = int(nb.sum()) * Hkv
+        select = total_pages * (2 * d * s + 4 + 8) + q_bytes + sel_bytes
+    last_valid = seq - (nb - 1) * P
+    meta = int(sum(int(v) * d * s + 2 * d * s for v in last_valid)) * Hkv
+    return dict(decode=decode, select=select, meta=meta, total=decode + select + meta, kv=kv)
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed"
+        if not rows:
+            rows = [s for _, s in self.samples]
+            window = "run"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows), "window": window}
+
+
+# ------------------------------------------------------------ references --
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, or None
+    if the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    src = os.path.join(ROOT, "query_aware_sparse_kv_gb300", "csrc", "decode.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = re.search(r"decode_cu_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != sha:
+        return None
+    return int(m.group(1))
+
+
+# ------------------------------------------------------------ distributed --
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_spec(spec: W.Spec, rank: int) -> W.Spec:
+    """Rank r decodes its own batch of the same shape (weak scaling)."""
+    import dataclasses
+
+    return dataclasses.replace(spec, seed=spec.seed + 1000 * rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------- oracle --
+def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_target_s: float | None = None):
+    """Times the CPU oracle (scores, top-K, attention) on a bounded sample of
+    rows.  Returns (steps/s, cores, sample description, rows per step used)."""
+    import oracle
+
+    spec = inputs["spec"]
+    n_rows = spec.batch * spec.num_kv_heads
+    meta = None
+    if spec.top_k is not None:
+        ids, vt = oracle.all_pages(inputs)
+        meta = oracle.meta(inputs["k_pool"], ids, vt)
+    rng = np.random.default_rng(0)
+    # calibrate on a small sample
+    calib = rng.choice(n_rows, size=min(n_rows, max(threads, 8)), replace=False).astype(np.int32)
+    t0 = time.perf_counter()
+    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv_cpu[0], threads=threads)
+    dt = time.perf_counter() - t0
+    rows_per_s = len(calib) / max(dt, 1e-9)
+    cores = int(res["threads"])
+    per_step = step_target_s if step_target_s is not None else budget_s
+    n = int(min(n_rows, max(1, rows_per_s * per_step)))
+    done_rows, t_total, steps = 0, 0.0, 0
+    while t_total < budget_s or steps == 0:
+        rows = rng.choice(n_rows, size=n, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv_cpu[steps % len(qv_cpu)], threads=threads)
+        t_total += time.perf_counter() - t0
+        done_rows += n
+        steps += 1
+        if step_target_s is not None:
+            break
+    steps_per_s = (done_rows / n_rows) / t_total
+    sample = (f"{done_rows} of {n_rows} (sequence, KV head) rows per full step, full step = "
+              f"scores + top-K + attention; {cores} OpenMP threads; {t_total:.2f} s")
+    return steps_per_s, cores, sample, n
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    spec = W.spec_for(args.workload)
+    inputs = W.make_inputs(spec)
+    qv = W.q_variants(inputs, N_Q_VARIANTS)
+    threads = os.cpu_count() or 1
+    # each of the K steps is a bounded sample sized so the run lasts about two minutes
+    per_step = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+    import oracle
+
+    meta = None
+    if spec.top_k is not None:
+        ids, vt = oracle.all_pages(inputs)
+        meta = oracle.meta(inputs["k_pool"], ids, vt)
+    n_rows = spec.batch * spec.num_kv_heads
+    rng = np.random.default_rng(0)
+    calib = np.arange(min(n_rows, max(threads, 8)), dtype=np.int32)
+    t0 = time.perf_counter()
+    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv[0], threads=threads)
+    rows_per_s = len(calib) / (time.perf_counter() - t0)
+    n = int(min(n_rows, max(1, rows_per_s * per_step)))
+    for i in range(args.warmup):
+        oracle.step(inputs, rows=rng.choice(n_rows, size=n, replace=False).astype(np.int32), meta_arr=meta,
+                    q=qv[i % N_Q_VARIANTS], threads=threads)
+    t_total = 0.0
+    for i in range(args.steps):
+        rows = rng.choice(n_rows, size=n, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv[i % N_Q_VARIANTS], threads=threads)
+        t_total += time.perf_counter() - t0
+    steps_per_s = (args.steps * n / n_rows) / t_total
+    cores = int(res["threads"])
+    sample = (f"each step: {n} of {n_rows} random (sequence, KV head) rows (scores + top-K + attention), "
+              f"scaled to full steps; {cores} OpenMP threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / steps_per_s,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(spec),
+        "cpu_baseline": {"value": steps_per_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": steps_per_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(spec: W.Spec) -> dict:
+    desc = {
+        "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
+        "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
+        "long_context": "long-context GQA decode, 64K-128K tokens, query-aware top-K paged KV",
+        "shared_prefix": "shared-prefix dense paged decode (all pages)",
+        "tiny": "tiny correctness batch",
+    }.get(spec.name, spec.name)
+    return {"workload": desc, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
+            "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page_size": spec.page_size,
+            "seq_len": list(spec.seq_len_range) if spec.seq_len_range else
+            (list(spec.seq_lens)[:1] if spec.seq_lens else None),
+            "top_k": spec.top_k, "kv_dtype": str(spec.kv_dtype).replace("torch.", ""),
+            "q_dtype": str(spec.q_dtype).replace("torch.", ""),
+            "l2": "inputs larger than L2 (KV pool and metadata) + 16 rotating query variants"}
+
+
+# ------------------------------------------------------------------ main --
+def run_gpu(args):
+    import query_aware_sparse_kv_gb300 as qskv
+    from query_aware_sparse_kv_gb300 import build as qbuild
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        qbuild.build()
+    barrier(world)
+    qskv.load()
+
+    spec = shard_spec(W.spec_for(args.workload), rank)
+    inputs = W.make_inputs(spec)
+    qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
+    dec = qskv.from_inputs(inputs, device=dev)
+    qv = qv_cpu.to(dev)
+    ids, vt = W.all_pages(inputs)
+    dec.build_meta(ids.to(dev), vt.to(dev))
+    last_ids, last_valid = (t.to(dev) for t in W.last_pages(inputs))
+    dec.check()
+    stream = torch.cuda.current_stream()
+
+    # algorithmic bytes: average over the query variants' selections
+    acc = []
+    for v in range(N_Q_VARIANTS):
+        if spec.top_k is not None:
+            dec.select(q=qv[v])
+            torch.cuda.synchronize()
+            acc.append(step_bytes(inputs, dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy()))
+        else:
+            acc.append(step_bytes(inputs, None, None))
+            break
+    nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
+
+    def one_step(i, ev=None):
+        v = i % N_Q_VARIANTS
+        dec.build_meta(last_ids, last_valid)
+        if spec.top_k is not None:
+            dec.select(q=qv[v])
+        if ev is not None:
+            ev[0].record(stream)
+        dec.decode(q=qv[v])
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        one_step(i)
+    dec.check()
+    torch.cuda.synchronize()
+
+    gpu_id = str(local)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(i, dec_ev[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    clocks = None
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(wall0, wall1)
+    dec.check()
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1000.0)
+
+    # end to end through the public API: pinned host q in, host out back, every step
+    e2e_steps = min(args.steps, 500)
+    q_host = qv_cpu.pin_memory()
+    q_dev = torch.empty_like(qv[0])
+    out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        q_dev.copy_(q_host[i % N_Q_VARIANTS], non_blocking=True)
+        dec.build_meta(last_ids, last_valid)
+        if spec.top_k is not None:
+            dec.select(q=q_dev)
+        dec.decode(q=q_dev)
+        out_host.copy_(dec.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    dec.check()
+    e2e_value = world * e2e_steps / e2e_s
+
+    if rank != 0:
+        return 0
+    peaks = measured_peaks()
+    decode_gbs = nbytes["decode"] / (decode_ms * 1e-3) / 1e9
+    step_gbs = nbytes["total"] / (ms_per_step * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        sps, cores, sample, _ = oracle_sample(inputs, qv_cpu, budget_s=args.cpu_budget,
+                                              threads=os.cpu_count() or 1)
+        cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": workload_config(spec),
+        "effective_gbs": step_gbs,
+        "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
+        "bytes_per_step": nbytes,
+        "roofline": {"kernel": "decode_bf16_kernel (qskv_sparse_paged_decode)", "bound": "hbm",
+                     "achieved": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": decode_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "decode_ms": decode_ms, "bytes_per_launch": nbytes["decode"],
+                     "traffic": ncu_traffic(args.workload)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps,
+                "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "gpu_launches": 3 * args.steps if spec.top_k is not None else 2 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["qskv", "reference"], default="qskv")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle timing for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

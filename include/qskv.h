@@ -1,0 +1,180 @@
+/*
+ * qskv.h -- query-aware sparse paged KV decode for GB300 (sm_103a).
+ *
+ * C ABI of libqskv.so.  Three calls make one decode step:
+ *
+ *   qskv_kv_meta_build       per-page min/max key metadata          (cache phase)
+ *   qskv_page_select         bound score of every page + top-K      (indexer phase)
+ *   qskv_sparse_paged_decode softmax(q K^T * scale) V over the selected pages,
+ *                            split over warps and merged by log-sum-exp
+ *
+ * Sources (web pages on the method):
+ *   TinyServe query-aware page selection article: s1 (fixed-size KV pages,
+ *   selection per page), s2.1 (metadata m_j, M_j), s2.2 (bound score),
+ *   s2.3 (score all pages, top-K, load only those pages, attend), s5.3
+ *   (metadata refreshed every decode step).
+ *   Vortex sparse-attention digest, method overview item 1: a query-
+ *   independent cache phase (per-block summaries) and a query-dependent
+ *   indexer phase (score, top-K, attend).
+ *   CS336 Lecture 10 "Inference": s2.3 (decode attention), s5.1 (GQA: G query
+ *   heads share one KV head), s9.2 (PagedAttention block table; shared
+ *   prefixes map to the same physical blocks).
+ *   Quail AI-SQL engine article, "the inference engine as an execution
+ *   engine": partial attention results combined by log-sum-exp rescaling.
+ *
+ * Layouts (row-major, all on the device unless stated):
+ *   k_pool, v_pool  [num_pool_pages][num_kv_heads][page_size][head_dim]  (kv dtype)
+ *   meta            [num_pool_pages][num_kv_heads][2][head_dim]          (kv dtype)
+ *                   row 0 = element-wise min m, row 1 = max M, over the
+ *                   page's valid tokens
+ *   q               [batch][num_q_heads][head_dim]                       (q dtype)
+ *   page_table      [batch][max_pages] int32 physical page ids; entries
+ *                   at or past ceil(seq_len / page_size) are never read;
+ *                   several rows may name the same physical page (prefix sharing)
+ *   seq_lens        [batch] int32 tokens per sequence, 0 <= seq_len <= max_pages*page_size
+ *   selected        [batch][num_kv_heads][top_k] int32 logical page indices,
+ *                   ascending, -1 padded
+ *   n_selected      [batch][num_kv_heads] int32
+ *   scores          [batch][num_kv_heads][max_pages] fp32
+ *   out             [batch][num_q_heads][head_dim] fp32
+ *   lse             [batch][num_q_heads] fp32 natural-log log-sum-exp of the
+ *                   scaled logits
+ * Query head h reads KV head h / G, G = num_q_heads / num_kv_heads.
+ *
+ * Supported: head_dim 64 or 128; page_size 16 or 32; G in {1, 2, 4, 8};
+ * kv dtype fp32 or bf16 (meta has the kv dtype); q dtype fp32 or bf16.
+ * Every device pointer that is read or written in 16-byte vectors (q, k_pool,
+ * v_pool, meta, out) must be 16-byte aligned; int32 arrays 4-byte aligned.
+ *
+ * Ownership: the caller allocates every buffer, including the workspace.  The
+ * library allocates no device memory, keeps no state besides a per-device
+ * attribute cache, launches only on the given stream (a cudaStream_t passed
+ * as void*, NULL for the legacy default stream) and never synchronises,
+ * except in qskv_get_error.
+ *
+ * Errors: a call returns a non-OK status before any launch when an argument
+ * fails a host check (qskv_last_error_message() then says which), or
+ * QSKV_ERR_CUDA when a launch fails.  Problems only the device can see (a
+ * page id outside [0, num_pool_pages), a selected index outside the
+ * sequence, seq_len beyond the table, a valid-token count outside
+ * [1, page_size], a wait that timed out) never trap: the offending page is
+ * skipped and a flag is raised in the workspace, which qskv_get_error reports.
+ * Inputs must be finite except in slots past seq_len, which are never used.
+ */
+#ifndef QSKV_H
+#define QSKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSKV_OK = 0,
+    QSKV_ERR_INVALID_ARG = 1,  /* a host-side argument check failed */
+    QSKV_ERR_UNSUPPORTED = 2,  /* shape or dtype outside the supported set */
+    QSKV_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
+    QSKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    QSKV_ERR_DEVICE_INDEX = 5, /* the device met an out-of-range index (page skipped) */
+    QSKV_ERR_DEVICE_TIMEOUT = 6 /* a bounded device wait gave up (work abandoned) */
+} qskv_status;
+
+typedef enum { QSKV_F32 = 0, QSKV_BF16 = 1 } qskv_dtype;
+
+typedef struct {
+    int32_t batch;          /* B: sequences */
+    int32_t num_q_heads;    /* Hq */
+    int32_t num_kv_heads;   /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;       /* d */
+    int32_t page_size;      /* P: tokens per page */
+    int32_t max_pages;      /* page_table row length */
+    int32_t num_pool_pages; /* physical pages in k_pool / v_pool / meta */
+} qskv_shape;
+
+/*
+ * Bytes of workspace one decode step needs on the current device (the three
+ * calls may share one buffer).  The workspace must be 256-byte aligned and
+ * zero-filled once before first use (e.g. cudaMemsetAsync); every call
+ * leaves it ready for the next one.  It holds the device error word, per-row
+ * completion counters, a score buffer for callers that pass none, and the
+ * split partial outputs (one slot per row plus one per decode warp).  Calls
+ * sharing a workspace must not run concurrently on different streams.
+ * Returns 0 if the shape is invalid or the device cannot be queried.
+ */
+size_t qskv_workspace_size(const qskv_shape *shape);
+
+/*
+ * Metadata build (TinyServe s2.1; refreshed every decode step, s5.3; the
+ * cache phase of the Vortex two-phase split).
+ * For each listed physical page p = page_ids[i] and every KV head g:
+ *   meta[p][g][0][c] = min over t < valid_tokens[i] of k_pool[p][g][t][c]
+ *   meta[p][g][1][c] = max over the same tokens
+ * exactly, in the kv dtype.  Other pages' metadata is left untouched.  At
+ * prefill list every page; at a decode step list each sequence's last page.
+ *   page_ids, valid_tokens  [n_pages] int32 device arrays
+ *   n_pages >= 0 (0 is a no-op)
+ * Device errors: page id out of range or valid_tokens outside [1, page_size]
+ * -> that entry is skipped, QSKV_ERR_DEVICE_INDEX is flagged.
+ */
+qskv_status qskv_kv_meta_build(const void *k_pool, qskv_dtype kv_dtype, const qskv_shape *shape,
+                               const int32_t *page_ids, const int32_t *valid_tokens, int32_t n_pages,
+                               void *meta, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Page selection (TinyServe s2.2-2.3; the indexer phase of the Vortex split).
+ * For sequence b, KV head g and each logical page j < n_b = ceil(seq_len/P),
+ * with p = page_table[b][j] and m, M the page's metadata:
+ *   s_h(j)  = sum_c q[b][h][c] * (q[b][h][c] > 0 ? M[c] : m[c])  for each
+ *             query head h of the group (an upper bound of max_t q_h . k_t)
+ *   S(j)    = max over the group's heads of s_h(j)
+ * selected[b][g][0..n) = the n = min(top_k, n_b) pages of largest S(j)
+ * (equal scores: the lower page index wins), in ascending page order, -1 past
+ * n; n_selected[b][g] = n.  Scores are computed in fp32; when `scores` is
+ * non-NULL, S(j) is written to scores[b][g][j] for every j < n_b (entries
+ * past n_b are left untouched), else a workspace buffer is used.
+ * Device errors: a bad page id scores -inf and flags QSKV_ERR_DEVICE_INDEX.
+ */
+qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta, qskv_dtype meta_dtype,
+                             const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
+                             int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse paged decode attention (TinyServe s2.3 stages 3-4; split-K with a
+ * log-sum-exp merge, Quail / flash decoding).
+ * For each query head h of sequence b (KV head g = h / G), over the tokens
+ * t < seq_len of the pages listed in selected[b][g][0..n_selected[b][g]):
+ *   l_t = sm_scale * (q_h . k_t),  out[b][h] = sum_t softmax(l)_t v_t,
+ *   lse[b][h] = log sum_t exp(l_t).
+ * selected == NULL means every page j < n_b (exact dense paged decode);
+ * n_selected and top_k are then ignored.  sm_scale == 0 means 1/sqrt(d).
+ * A sequence with no token gives out = 0 and lse = -inf.  lse may be NULL.
+ * Device errors: a bad page id or selected index skips that page and flags
+ * QSKV_ERR_DEVICE_INDEX.
+ */
+qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
+                                     qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                     const qskv_shape *shape, const int32_t *selected, const int32_t *n_selected,
+                                     int32_t top_k, float sm_scale, float *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, reads and clears the workspace's device error flags,
+ * and returns QSKV_OK, QSKV_ERR_DEVICE_INDEX, QSKV_ERR_DEVICE_TIMEOUT or
+ * QSKV_ERR_CUDA.  The only call that blocks the host.
+ */
+qskv_status qskv_get_error(void *workspace, void *stream);
+
+/* Static, human-readable name of a status. */
+const char *qskv_status_string(qskv_status status);
+
+/* Detail of the last non-OK status returned on this host thread ("" if none). */
+const char *qskv_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSKV_H */

@@ -1,1 +1,20 @@
-"""Query-aware sparse paged KV decode for GB300 (sm_103a)."""
+"""Query-aware sparse paged KV decode for GB300 (sm_103a).
+
+The computation lives in libqskv.so (CUDA kernels behind the C ABI declared
+in include/qskv.h); this package is its binding:
+
+  kv_meta_build        per-page min/max key metadata
+  page_select          bound score of every page and top-K per (sequence, KV head)
+  sparse_paged_decode  split-K attention over the selected pages, LSE merge
+
+plus ``PagedDecoder`` (buffer plumbing for a whole step) and ``workloads``
+(seeded synthetic inputs).  Nothing here computes on the CPU: without the
+built library every call raises.
+"""
+from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, get_error, kv_meta_build,
+                      last_error_message, load, make_shape, page_select, sparse_paged_decode, workspace_size)
+from .engine import PagedDecoder, from_inputs
+
+__all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "get_error", "kv_meta_build",
+           "last_error_message", "load", "make_shape", "page_select", "sparse_paged_decode", "workspace_size",
+           "PagedDecoder", "from_inputs"]

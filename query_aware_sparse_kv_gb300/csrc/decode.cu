@@ -1,0 +1,571 @@
+// Split-K sparse paged decode attention with a log-sum-exp merge.
+//
+// TinyServe query-aware page selection, s2.3 stages 3-4: only the selected
+// pages are loaded from HBM and attention runs while they stream in; s3.1:
+// later pages are prefetched while the current one is processed.  The split
+// over workers and the merge of their partial results by log-sum-exp
+// rescaling follow the Quail AI-SQL engine article (partial attention
+// combined as in flash decoding) and CS336 Lecture 10 s9.2 (fused paged
+// reads, FlashDecoding).
+//
+// Work decomposition.  A "unit" is one slot of one (sequence, KV head) row:
+// row r has `slots_per_row` units (top_k, or max_pages for dense decode),
+// unit r*slots + s names the s-th selected page of the row (empty past
+// n_selected).  The units are cut into equal contiguous ranges, one per warp
+// of a persistent grid, so every warp streams about the same number of pages
+// whatever the row lengths.  A warp keeps an online softmax per query head of
+// the group; at the end of each row it owns a piece of, it either writes the
+// final output (it owns the whole row) or a normalised partial output with
+// its log-sum-exp into slot (row + warp) of the workspace and takes a ticket
+// on the row; the warp that completes the row merges the partials.  No warp
+// ever waits for another.
+//
+// bf16 KV (tensor cores).  Each warp runs its own pipeline of `stages`
+// shared-memory buffers filled by 2-D TMA tiled loads (16 tokens x 64 dims
+// per box, 128-byte swizzle) that complete on one mbarrier per buffer; lane 0
+// issues, the whole warp consumes, and the buffer is refilled as soon as the
+// warp is done with it.  Per 16-token sub-tile:
+//   S^T (16 tokens x 8 heads) = K_tile . Q^T       mma.sync m16n8k16, K via ldmatrix
+//   online softmax per head column (exp2, scale folded with log2 e)
+//   P^T as the B operand: bf16 pack + movmatrix.trans of the S^T fragment
+//   O^T (d x 8 heads)    += V_tile^T . P^T         V via ldmatrix.trans
+// Query heads sit on the n = 8 axis (G <= 8), so per-head state lines up
+// with the accumulator columns.  Token rows past seq_len are masked to -inf
+// before the softmax and the matching V rows are zeroed in shared memory
+// (0 * NaN would poison the product).  fp32 queries are split into hi + lo
+// bf16 halves (two mma per k-step).  Probabilities are rounded to bf16 for
+// the P.V product and the same rounded values feed the softmax denominator.
+//
+// fp32 KV runs a CUDA-core kernel with the same decomposition and merge.
+#include "qskv_device.cuh"
+#include "qskv_internal.h"
+
+namespace qskv {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+// (physical page << 6 | valid tokens) of unit u, or -1 when the unit is
+// empty or names an out-of-range page (flagged).
+__device__ __forceinline__ int unit_code(const DecodeArgs &a, int64_t u, int64_t u_end) {
+    if (u >= u_end) return -1;
+    const int row = int(u / a.slots_per_row);
+    const int slot = int(u % a.slots_per_row);
+    const int b = row / a.num_kv_heads;
+    int seq = a.seq_lens[b];
+    const int cap = a.max_pages * a.page_size;
+    if (seq < 0 || seq > cap) {
+        raise_error(a.flags, kErrSeqLen);
+        seq = seq < 0 ? 0 : cap;
+    }
+    const int n_b = (seq + a.page_size - 1) / a.page_size;
+    int j;
+    if (a.selected) {
+        int ns = a.n_selected[row];
+        const int lim = min(a.top_k, n_b);
+        if (ns < 0 || ns > lim) {
+            raise_error(a.flags, kErrSelected);
+            ns = max(0, min(ns, lim));
+        }
+        if (slot >= ns) return -1;
+        j = a.selected[int64_t(row) * a.top_k + slot];
+        if (j < 0 || j >= n_b) {
+            raise_error(a.flags, kErrSelected);
+            return -1;
+        }
+    } else {
+        if (slot >= n_b) return -1;
+        j = slot;
+    }
+    const int p = a.page_table[int64_t(b) * a.max_pages + j];
+    if (p < 0 || p >= a.num_pool_pages) {
+        raise_error(a.flags, kErrPageId);
+        return -1;
+    }
+    return (p << 6) | min(a.page_size, seq - j * a.page_size);
+}
+
+// Warps whose unit ranges intersect row `row`.
+__device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t &w0, int64_t &w1) {
+    const int64_t first = int64_t(row) * a.slots_per_row;
+    const int64_t last = min(first + a.slots_per_row, a.total_units) - 1;
+    w0 = first / a.units_per_warp;
+    w1 = last / a.units_per_warp;
+}
+
+// One warp merges the partials of row `row` from warps w0..w1 (slots row+w).
+template <int D>
+__device__ void merge_row(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+    constexpr int V4 = D / 4;
+    for (int idx = lane; idx < G * V4; idx += 32) {
+        const int h = idx / V4, c4 = idx % V4;
+        float mx = -INFINITY;
+        for (int64_t w = w0; w <= w1; w++) mx = fmaxf(mx, __ldcg(a.part_lse + (row + w) * G + h));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
+        if (mx != -INFINITY) {
+            for (int64_t w = w0; w <= w1; w++) {
+                const int64_t slot = row + w;
+                const float wt = exp2f(__ldcg(a.part_lse + slot * G + h) - mx);
+                const float4 o = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (slot * G + h) * D) + c4);
+                den += wt;
+                acc.x = fmaf(wt, o.x, acc.x);
+                acc.y = fmaf(wt, o.y, acc.y);
+                acc.z = fmaf(wt, o.z, acc.z);
+                acc.w = fmaf(wt, o.w, acc.w);
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G + h;
+        reinterpret_cast<float4 *>(a.out + qh * D)[c4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (c4 == 0 && a.lse) a.lse[qh] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+    }
+}
+
+// After this warp wrote its partial for `row`: take a ticket; the last
+// contributor merges and re-arms the counter.
+template <int D>
+__device__ __forceinline__ void arrive_row(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
+    const int lane = threadIdx.x & 31;
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(a.tickets + row, 1) == int(w1 - w0);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence();
+        merge_row<D>(a, row, w0, w1);
+        if (lane == 0) a.tickets[row] = 0;
+    }
+}
+
+// ------------------------------------------------- bf16 KV, tensor cores --
+template <int D, bool QF32>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                       DecodeArgs a) {
+    constexpr int NB = D / 64;          // 64-dim boxes per token row
+    constexpr int BOX = 16 * 128;       // bytes of one box: 16 tokens x 128 B
+    constexpr int KVB = NB * BOX;       // K (or V) bytes of a 16-token sub-tile
+    constexpr int STAGE = 2 * KVB;
+    constexpr int NKS = D / 16;         // k-steps of Q.K^T, m-tiles of P.V
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kDecodeWarps][kMaxStages];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = lane & 3, gid = lane >> 2;
+    const int S = a.stages;
+    const int G = a.group;
+    const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
+    const int64_t u_begin = gw * a.units_per_warp;
+    const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
+    if (u_begin >= u_end) return;
+
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) +
+                    size_t(warp) * S * STAGE;
+    uint64_t *bar = bars[warp];
+    if (lane == 0) {
+        for (int s = 0; s < S; s++) mbar_init(bar + s, 1);
+        mbar_fence_init();
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    __syncwarp();
+
+    // Codes of units [wbase, wbase + 64): lane i holds units wbase+i and wbase+32+i.
+    int64_t wbase = u_begin;
+    int code_cur = unit_code(a, wbase + lane, u_end);
+    int code_nxt = unit_code(a, wbase + 32 + lane, u_end);
+    auto code_of = [&](int64_t u) -> int {
+        const int k = int(u - wbase);
+        const int c0 = __shfl_sync(0xffffffffu, code_cur, k & 31);
+        const int c1 = __shfl_sync(0xffffffffu, code_nxt, k & 31);
+        return k < 32 ? c0 : c1;
+    };
+
+    // ---------------- producer: lane 0 issues TMA for the next sub-tiles
+    int64_t pu = u_begin;
+    int psub = 0, ps = 0;
+    uint32_t issued = 0, consumed = 0;
+    auto produce = [&]() {
+        while (int(issued - consumed) < S && pu < u_end && pu - wbase < 64) {
+            const int code = code_of(pu);
+            if (code < 0) {
+                pu++;
+                psub = 0;
+                continue;
+            }
+            const int valid = code & 63, phys = code >> 6;
+            const int g = int(pu / a.slots_per_row) % a.num_kv_heads;
+            if (lane == 0) {
+                uint8_t *st = ring + size_t(ps) * STAGE;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar + ps, STAGE);
+                const int y = (phys * a.num_kv_heads + g) * a.page_size + psub * 16;
+#pragma unroll
+                for (int nb = 0; nb < NB; nb++) {
+                    tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y, bar + ps);
+                    tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y, bar + ps);
+                }
+            }
+            issued++;
+            ps = ps + 1 == S ? 0 : ps + 1;
+            if (++psub == (valid + 15) >> 4) {
+                pu++;
+                psub = 0;
+            }
+        }
+    };
+
+    // ---------------- consumer state (per row)
+    int cur_row = -1;
+    float o[NKS][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2t, 2t+1
+    uint32_t qb[NKS][2], ql[NKS][2];
+
+    auto start_row = [&](int row) {
+        const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < NKS; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        const bool ok = gid < G;
+        const int64_t qoff = (int64_t(b) * a.num_q_heads + int64_t(g) * G + (ok ? gid : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ks++) {
+            const int k0 = ks * 16 + 2 * t;
+            if (QF32) {
+                const float *q = static_cast<const float *>(a.q) + qoff;
+                const float2 x0 = *reinterpret_cast<const float2 *>(q + k0);
+                const float2 x1 = *reinterpret_cast<const float2 *>(q + k0 + 8);
+                const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
+                qb[ks][0] = ok ? h0 : 0u;
+                qb[ks][1] = ok ? h1 : 0u;
+                ql[ks][0] = ok ? pack_bf16x2(x0.x - bf16_lo_to_float(h0), x0.y - bf16_hi_to_float(h0)) : 0u;
+                ql[ks][1] = ok ? pack_bf16x2(x1.x - bf16_lo_to_float(h1), x1.y - bf16_hi_to_float(h1)) : 0u;
+            } else {
+                const uint32_t *q = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff);
+                qb[ks][0] = ok ? q[k0 / 2] : 0u;
+                qb[ks][1] = ok ? q[(k0 + 8) / 2] : 0u;
+            }
+        }
+    };
+
+    auto finish_row = [&](int row) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const float e0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY, e1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+        const int h0 = 2 * t, h1 = 2 * t + 1;
+        int64_t w0, w1;
+        row_warps(a, row, w0, w1);
+        float *dst;
+        int64_t ldh;  // floats between heads
+        if (w0 == w1) {
+            const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+            const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+            dst = a.out + qh * D;
+            ldh = D;
+            if (a.lse && gid == 0) {
+                if (h0 < G) a.lse[qh + h0] = e0 * kLn2;
+                if (h1 < G) a.lse[qh + h1] = e1 * kLn2;
+            }
+        } else {
+            const int64_t slot = row + gw;
+            dst = a.part_o + slot * G * D;
+            ldh = D;
+            if (gid == 0) {
+                if (h0 < G) a.part_lse[slot * G + h0] = e0;
+                if (h1 < G) a.part_lse[slot * G + h1] = e1;
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < NKS; mt++) {
+            const int d0 = mt * 16 + gid;
+            if (h0 < G) {
+                dst[h0 * ldh + d0] = o[mt][0] * i0;
+                dst[h0 * ldh + d0 + 8] = o[mt][2] * i0;
+            }
+            if (h1 < G) {
+                dst[h1 * ldh + d0] = o[mt][1] * i1;
+                dst[h1 * ldh + d0 + 8] = o[mt][3] * i1;
+            }
+        }
+        if (w0 != w1) arrive_row<D>(a, row, w0, w1);
+    };
+
+    // ---------------- main loop
+    int64_t cu = u_begin;
+    int csub = 0, cs = 0;
+    uint32_t cphase = 0;
+    bool aborted = false;
+    produce();
+    while (cu < u_end) {
+        if (cu - wbase >= 32) {
+            wbase += 32;
+            code_cur = code_nxt;
+            code_nxt = unit_code(a, wbase + 32 + lane, u_end);
+        }
+        produce();
+        const int row = int(cu / a.slots_per_row);
+        if (row != cur_row) {
+            if (cur_row >= 0) finish_row(cur_row);
+            cur_row = row;
+            start_row(row);
+        }
+        const int code = code_of(cu);
+        if (code < 0) {
+            cu++;
+            csub = 0;
+            continue;
+        }
+        const int valid = code & 63;
+        const int vsub = min(16, valid - csub * 16);
+        if (!mbar_wait_bounded(bar + cs, cphase, kWaitLimitNs)) {
+            if (lane == 0) raise_error(a.flags, kErrTimeout);
+            aborted = true;
+            break;
+        }
+        uint8_t *st = ring + size_t(cs) * STAGE;
+        if (vsub < 16) {  // zero V rows past the sequence end (they may hold NaN)
+            uint4 *vrow = reinterpret_cast<uint4 *>(st + KVB);
+            const int n = (16 - vsub) * 8;
+            for (int i = lane; i < NB * n; i += 32) {
+                const int nb = i / n, r = vsub + (i % n) / 8, c = i % 8;
+                vrow[(nb * BOX + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+        const uint32_t kb = smem_u32(st), vb = kb + KVB;
+
+        // S^T = K . Q^T
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mat = lane >> 3;
+            const int r = (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+            for (int ks = 0; ks < NKS; ks++) {
+                const int c = (ks & 3) * 2 + (mat >> 1);
+                uint32_t af[4];
+                ldmatrix_x4(af, kb + (ks >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
+                mma_bf16_16816(sacc, af, qb[ks][0], qb[ks][1]);
+                if (QF32) mma_bf16_16816(sacc, af, ql[ks][0], ql[ks][1]);
+            }
+        }
+        // online softmax; sacc = [tok gid][h0], [gid][h1], [gid+8][h0], [gid+8][h1]
+        const float sc = a.scale_log2;
+        const float s0 = gid < vsub ? sacc[0] * sc : -INFINITY;
+        const float s1 = gid < vsub ? sacc[1] * sc : -INFINITY;
+        const float s2 = gid + 8 < vsub ? sacc[2] * sc : -INFINITY;
+        const float s3 = gid + 8 < vsub ? sacc[3] * sc : -INFINITY;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        const uint32_t x0 = pack_bf16x2(exp2f(s0 - n0), exp2f(s1 - n1));
+        const uint32_t x1 = pack_bf16x2(exp2f(s2 - n0), exp2f(s3 - n1));
+        l0 = l0 * al0 + (bf16_lo_to_float(x0) + bf16_lo_to_float(x1));
+        l1 = l1 * al1 + (bf16_hi_to_float(x0) + bf16_hi_to_float(x1));
+#pragma unroll
+        for (int mt = 0; mt < NKS; mt++) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
+        // O^T += V^T . P^T
+        {
+            const int mat = lane >> 3;
+            const int r = (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+            for (int mt = 0; mt < NKS; mt++) {
+                const int c = (mt & 3) * 2 + (mat & 1);
+                uint32_t af[4];
+                ldmatrix_x4_trans(af, vb + (mt >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
+                mma_bf16_16816(o[mt], af, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        consumed++;
+        if (++cs == S) {
+            cs = 0;
+            cphase ^= 1u;
+        }
+        if (++csub == (valid + 15) >> 4) {
+            cu++;
+            csub = 0;
+        }
+    }
+    if (aborted) {
+        // let the copies already issued land before the CTA's memory is released
+        while (consumed != issued) {
+            mbar_wait_bounded(bar + cs, cphase, kWaitLimitNs);
+            consumed++;
+            if (++cs == S) {
+                cs = 0;
+                cphase ^= 1u;
+            }
+        }
+        return;
+    }
+    if (cur_row >= 0) finish_row(cur_row);
+}
+
+// --------------------------------------------------- fp32 KV, CUDA cores --
+template <int D, bool QF32>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeArgs a) {
+    constexpr int PL = D / 32;  // dims per lane: lane + 32 * i
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.group;
+    const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
+    const int64_t u_begin = gw * a.units_per_warp;
+    const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
+    if (u_begin >= u_end) return;
+    float q[8][PL], o[8][PL], m[8], l[8];
+    int cur_row = -1;
+
+    auto start_row = [&](int row) {
+        const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+#pragma unroll
+        for (int h = 0; h < 8; h++) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+            const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G + (h < G ? h : 0);
+#pragma unroll
+            for (int i = 0; i < PL; i++) {
+                o[h][i] = 0.f;
+                const int64_t qi = qh * D + lane + 32 * i;
+                q[h][i] = QF32 ? static_cast<const float *>(a.q)[qi]
+                               : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.q)[qi]);
+            }
+        }
+    };
+    auto finish_row = [&](int row) {
+        int64_t w0, w1;
+        row_warps(a, row, w0, w1);
+        const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+        const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+        const int64_t slot = row + gw;
+#pragma unroll
+        for (int h = 0; h < 8; h++) {
+            if (h >= G) break;
+            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+            const float e = l[h] > 0.f ? m[h] + log2f(l[h]) : -INFINITY;
+            float *dst = (w0 == w1) ? a.out + (qh + h) * D : a.part_o + (slot * G + h) * D;
+#pragma unroll
+            for (int i = 0; i < PL; i++) dst[lane + 32 * i] = o[h][i] * inv;
+            if (lane == 0) {
+                if (w0 == w1) {
+                    if (a.lse) a.lse[qh + h] = e * kLn2;
+                } else {
+                    a.part_lse[slot * G + h] = e;
+                }
+            }
+        }
+        if (w0 != w1) arrive_row<D>(a, row, w0, w1);
+    };
+
+    for (int64_t u = u_begin; u < u_end; u++) {
+        const int row = int(u / a.slots_per_row);
+        if (row != cur_row) {
+            if (cur_row >= 0) finish_row(cur_row);
+            cur_row = row;
+            start_row(row);
+        }
+        const int code = unit_code(a, u, u_end);
+        if (code < 0) continue;
+        const int valid = code & 63, phys = code >> 6;
+        const int g = row % a.num_kv_heads;
+        const int64_t tile = (int64_t(phys) * a.num_kv_heads + g) * a.page_size * D;
+        const float *kt = static_cast<const float *>(a.k_pool) + tile;
+        const float *vt = static_cast<const float *>(a.v_pool) + tile;
+        for (int tok = 0; tok < valid; tok++) {
+            float kv[PL], vv[PL];
+#pragma unroll
+            for (int i = 0; i < PL; i++) {
+                kv[i] = kt[tok * D + lane + 32 * i];
+                vv[i] = vt[tok * D + lane + 32 * i];
+            }
+#pragma unroll
+            for (int h = 0; h < 8; h++) {
+                if (h >= G) break;
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < PL; i++) dot = fmaf(q[h][i], kv[i], dot);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                const float s = dot * a.scale_log2;
+                const float mn = fmaxf(m[h], s);
+                const float al = exp2f(m[h] - mn), p = exp2f(s - mn);
+                m[h] = mn;
+                l[h] = l[h] * al + p;
+#pragma unroll
+                for (int i = 0; i < PL; i++) o[h][i] = fmaf(p, vv[i], o[h][i] * al);
+            }
+        }
+    }
+    if (cur_row >= 0) finish_row(cur_row);
+}
+
+template <int D, bool QF32>
+cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
+                        cudaStream_t stream) {
+    const size_t smem = decode_smem_bytes(D, a.stages);
+    static size_t configured[64] = {0};  // dynamic smem limit already set, per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || configured[dev] < smem) {
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_bf16_kernel<D, QF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = smem;
+    }
+    decode_bf16_kernel<D, QF32><<<grid.ctas, kDecodeWarps * 32, smem, stream>>>(*tk, *tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_stages(int head_dim) { return head_dim == 128 ? 3 : 6; }
+
+size_t decode_smem_bytes(int head_dim, int stages) {
+    const size_t stage = size_t(head_dim / 64) * 16 * 128 * 2;
+    return stage * size_t(stages) * kDecodeWarps + 1024;
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
+                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream) {
+    if (a.total_units == 0) return cudaSuccess;
+    const bool qf = q_dtype == kDtypeF32;
+    if (kv_dtype == kDtypeBf16) {
+        if (head_dim == 128) return qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
+                                       : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
+        return qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
+                  : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+    }
+    const dim3 g(grid.ctas), b(kDecodeWarps * 32);
+    if (head_dim == 128) {
+        if (qf) decode_simt_kernel<128, true><<<g, b, 0, stream>>>(a);
+        else decode_simt_kernel<128, false><<<g, b, 0, stream>>>(a);
+    } else {
+        if (qf) decode_simt_kernel<64, true><<<g, b, 0, stream>>>(a);
+        else decode_simt_kernel<64, false><<<g, b, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qskv

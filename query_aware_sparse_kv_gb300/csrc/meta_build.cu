@@ -1,0 +1,130 @@
+// Per-page min/max key metadata (TinyServe query-aware page selection, s2.1:
+// for every page the element-wise minimum m_j and maximum M_j of its key
+// vectors, 2d values per page; refreshed every decode step, s5.3).
+//
+// One warp per (listed page, KV head) tile of P x D keys.  Lanes read the
+// tile in 16-byte vectors, row-interleaved so a warp instruction covers whole
+// 128-byte lines; each lane keeps an element-wise running min and max of its
+// vector column, lanes holding the same column combine by shuffles, and the
+// two rows (min, max) are written back as 16-byte vectors.  Min/max are
+// exact, so the result is bit-identical to any other evaluation order (up to
+// the sign of zero).  Only tokens t < valid_tokens are read.
+#include "qskv_device.cuh"
+#include "qskv_internal.h"
+
+namespace qskv {
+namespace {
+
+struct Bf16Ops {
+    using vec = uint4;  // 8 bf16
+    static __device__ __forceinline__ vec lowest() {
+        const uint32_t w = 0xff80ff80u;  // -inf, -inf
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ vec highest() {
+        const uint32_t w = 0x7f807f80u;  // +inf, +inf
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+};
+
+struct F32Ops {
+    using vec = uint4;  // 4 fp32
+    static __device__ __forceinline__ vec lowest() {
+        const uint32_t w = 0xff800000u;
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ vec highest() {
+        const uint32_t w = 0x7f800000u;
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
+        return __float_as_uint(fminf(__uint_as_float(a), __uint_as_float(b)));
+    }
+    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
+        return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+    }
+};
+
+template <class Ops>
+__device__ __forceinline__ uint4 vmin4(uint4 a, uint4 b) {
+    return make_uint4(Ops::vmin(a.x, b.x), Ops::vmin(a.y, b.y), Ops::vmin(a.z, b.z), Ops::vmin(a.w, b.w));
+}
+template <class Ops>
+__device__ __forceinline__ uint4 vmax4(uint4 a, uint4 b) {
+    return make_uint4(Ops::vmax(a.x, b.x), Ops::vmax(a.y, b.y), Ops::vmax(a.z, b.z), Ops::vmax(a.w, b.w));
+}
+
+__device__ __forceinline__ uint4 shfl_xor4(uint4 v, int m) {
+    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                      __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+
+// ROW_BYTES = D * element size; CPR = 16-byte chunks per token row.
+template <class Ops, int ROW_BYTES>
+__global__ void __launch_bounds__(256) meta_build_kernel(MetaArgs a) {
+    constexpr int CPR = ROW_BYTES / 16;
+    constexpr int RP = 32 / CPR;  // token rows read in parallel by one warp
+    static_assert(CPR >= 1 && CPR <= 32 && 32 % CPR == 0, "row must be 16..512 bytes");
+    const int lane = threadIdx.x & 31;
+    const int64_t tile = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (tile >= int64_t(a.n_list) * a.num_kv_heads) return;
+    const int e = int(tile / a.num_kv_heads);
+    const int g = int(tile % a.num_kv_heads);
+    const int p = a.page_ids[e];
+    const int valid = a.valid_tokens[e];
+    if (p < 0 || p >= a.num_pool_pages) {
+        if (lane == 0) raise_error(a.flags, kErrPageId);
+        return;
+    }
+    if (valid < 1 || valid > a.page_size) {
+        if (lane == 0) raise_error(a.flags, kErrValid);
+        return;
+    }
+    const int c = lane % CPR;
+    const int r0 = lane / CPR;
+    const uint8_t *base =
+        static_cast<const uint8_t *>(a.k_pool) + ((int64_t(p) * a.num_kv_heads + g) * a.page_size) * ROW_BYTES;
+    uint4 mn = Ops::highest(), mx = Ops::lowest();
+#pragma unroll 4
+    for (int r = r0; r < valid; r += RP) {
+        const uint4 v = ldg_stream_v4(base + int64_t(r) * ROW_BYTES + c * 16);
+        mn = vmin4<Ops>(mn, v);
+        mx = vmax4<Ops>(mx, v);
+    }
+#pragma unroll
+    for (int off = CPR; off < 32; off <<= 1) {
+        mn = vmin4<Ops>(mn, shfl_xor4(mn, off));
+        mx = vmax4<Ops>(mx, shfl_xor4(mx, off));
+    }
+    uint8_t *out = static_cast<uint8_t *>(a.meta) + (int64_t(p) * a.num_kv_heads + g) * 2 * ROW_BYTES;
+    if (r0 == 0) *reinterpret_cast<uint4 *>(out + c * 16) = mn;
+    if (r0 == (RP > 1 ? 1 : 0)) *reinterpret_cast<uint4 *>(out + ROW_BYTES + c * 16) = mx;
+}
+
+}  // namespace
+
+cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream) {
+    const int64_t tiles = int64_t(a.n_list) * a.num_kv_heads;
+    if (tiles == 0) return cudaSuccess;
+    const int warps = 8;
+    const dim3 grid(unsigned((tiles + warps - 1) / warps));
+    const dim3 block(32 * warps);
+    if (kv_dtype == kDtypeBf16) {
+        if (head_dim == 128) meta_build_kernel<Bf16Ops, 256><<<grid, block, 0, stream>>>(a);
+        else meta_build_kernel<Bf16Ops, 128><<<grid, block, 0, stream>>>(a);
+    } else {
+        if (head_dim == 128) meta_build_kernel<F32Ops, 512><<<grid, block, 0, stream>>>(a);
+        else meta_build_kernel<F32Ops, 256><<<grid, block, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qskv

@@ -1,0 +1,402 @@
+// Page selection: bound score of every page, then the top-K pages per
+// (sequence, KV head) row.
+//
+// TinyServe query-aware page selection, s2.2: for query q and page j with
+// metadata (m_j, M_j), score_j = sum_i q[i] * (q[i] > 0 ? M_j[i] : m_j[i]),
+// an upper bound of the page's largest q.k.  s2.3: all pages are scored in
+// parallel ("metadata parallel scan"), then the K best are picked by a radix
+// pass in shared memory.  With grouped-query attention the row score is the
+// maximum of the G query heads' bounds (one selection per KV head).
+//
+// Scoring, bf16 metadata.  With q- = min(q, 0) and q+ = max(q, 0), the bound
+// is the dot product  [m_j | M_j] . [q- | q+]  (exact rewrite: for q > 0 the
+// first term is 0 and the second q M; for q < 0 the reverse; for q = 0 both
+// vanish).  So the scores of 16 pages for the G <= 8 heads of a group form a
+// (16 pages x 2d) . (2d x 8 heads) product: each warp runs it as m16n8k16
+// bf16 mma.sync with fp32 accumulation, the 16 metadata rows being the A
+// operand read straight from global memory in 16-byte vectors.  A and B use
+// the same permutation of the 2d-long k axis (each lane's 16-byte chunk feeds
+// two k-steps), which the dot product does not see.  bf16 products are exact
+// in fp32; fp32 queries are split as hi + lo bf16 pairs (two mma per step).
+// The same identity runs on CUDA cores (fp32 FMA) for fp32 metadata.
+//
+// Selection.  Each CTA scores up to 256 pages of one row and takes a ticket
+// on the row's counter; the CTA that arrives last (no waiting: the others
+// have already left) ranks the whole row.  Scores map to order-preserving
+// 32-bit keys; an MSB-first radix select over 8-bit digits, starting at the
+// highest bit where the row's keys differ, finds the K-th key; a stable
+// compaction in page order keeps every key above it and the lowest-index
+// keys equal to it.  The selected list comes out in ascending page order.
+#include "qskv_device.cuh"
+#include "qskv_internal.h"
+
+namespace qskv {
+namespace {
+
+// fp32 -> unsigned key with the same order; -0 and +0 map to one key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t shr32(uint32_t x, int s) { return s >= 32 ? 0u : (x >> s); }
+
+// Row bookkeeping shared by both score kernels.
+struct RowInfo {
+    int row, b, g, n_b;
+};
+
+__device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
+    RowInfo r;
+    r.row = blockIdx.y;
+    r.b = r.row / a.num_kv_heads;
+    r.g = r.row % a.num_kv_heads;
+    int seq = a.seq_lens[r.b];
+    const int cap = a.max_pages * a.page_size;
+    if (seq < 0 || seq > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
+        seq = seq < 0 ? 0 : cap;
+    }
+    r.n_b = (seq + a.page_size - 1) / a.page_size;
+    return r;
+}
+
+// --------------------------------------------------------------- select --
+template <int NT>
+__device__ __forceinline__ void block_exclusive_scan2(int &x, int &y, int *s_tmp /* 2*NT/32 */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ix = x, iy = y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int tx = __shfl_up_sync(0xffffffffu, ix, o);
+        const int ty = __shfl_up_sync(0xffffffffu, iy, o);
+        if (lane >= o) {
+            ix += tx;
+            iy += ty;
+        }
+    }
+    if (lane == 31) {
+        s_tmp[warp] = ix;
+        s_tmp[NT / 32 + warp] = iy;
+    }
+    __syncthreads();
+    int ox = 0, oy = 0;
+    for (int w = 0; w < warp; w++) {
+        ox += s_tmp[w];
+        oy += s_tmp[NT / 32 + w];
+    }
+    x = ox + ix - x;
+    y = oy + iy - y;
+    __syncthreads();
+}
+
+// Ranks one row's scores (all threads of the CTA take part).
+__device__ void select_row(const SelectArgs &a, int row, int n_b, const float *srow) {
+    constexpr int NT = kSelectThreads;
+    __shared__ uint32_t s_keys[kSelectKeyCap];
+    __shared__ uint32_t s_hist[256];
+    __shared__ int s_tmp[2 * NT / 32];
+    __shared__ uint32_t s_mm[2 * NT / 32];
+    __shared__ int s_pick[3];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = a.top_k;
+    int32_t *sel = a.selected + int64_t(row) * K;
+
+    if (K >= n_b) {  // every page is kept
+        for (int i = tid; i < K; i += NT) sel[i] = i < n_b ? i : -1;
+        if (tid == 0) a.n_selected[row] = n_b;
+        return;
+    }
+    const bool in_smem = n_b <= kSelectKeyCap;
+    auto key_at = [&](int i) -> uint32_t { return in_smem ? s_keys[i] : order_key(__ldcg(srow + i)); };
+
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < n_b; i += NT) {
+        const uint32_t k = order_key(__ldcg(srow + i));
+        if (in_smem) s_keys[i] = k;
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) {
+        s_mm[warp] = kmin;
+        s_mm[NT / 32 + warp] = kmax;
+    }
+    __syncthreads();
+    kmin = s_mm[0];
+    kmax = s_mm[NT / 32];
+    for (int w = 1; w < NT / 32; w++) {
+        kmin = min(kmin, s_mm[w]);
+        kmax = max(kmax, s_mm[NT / 32 + w]);
+    }
+
+    // Bits at and above `hi` are shared by every key of the row.
+    const uint32_t diff = kmin ^ kmax;
+    int hi = diff ? 32 - __clz(diff) : 0;
+    uint32_t prefix = hi >= 32 ? 0u : (kmax & ~((1u << hi) - 1u));
+    int need = K;  // keys still to take among those matching `prefix` above `hi`
+    int lo = hi;
+    while (hi > 0) {
+        lo = hi > 8 ? hi - 8 : 0;
+        const uint32_t mask = (1u << (hi - lo)) - 1u;
+        s_hist[tid] = 0u;  // NT == 256 bins
+        __syncthreads();
+        const uint32_t want = shr32(prefix, hi);
+        for (int i = tid; i < n_b; i += NT) {
+            const uint32_t k = key_at(i);
+            if (shr32(k, hi) == want) atomicAdd(&s_hist[(k >> lo) & mask], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t h[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                h[j] = s_hist[lane * 8 + j];
+                sum += h[j];
+            }
+            uint32_t suf = sum;  // inclusive suffix sum over lanes >= this one
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += t;
+            }
+            uint32_t acc = suf - sum;  // keys in higher lanes' bins
+#pragma unroll
+            for (int j = 7; j >= 0; j--) {
+                if (acc < uint32_t(need) && acc + h[j] >= uint32_t(need)) {
+                    s_pick[0] = lane * 8 + j;
+                    s_pick[1] = int(acc);
+                    s_pick[2] = int(h[j]);
+                }
+                acc += h[j];
+            }
+        }
+        __syncthreads();
+        const int bin = s_pick[0], above = s_pick[1], cnt = s_pick[2];
+        prefix |= uint32_t(bin) << lo;
+        need -= above;
+        __syncthreads();
+        if (cnt == need) break;  // the whole bucket is taken: no tie to cut
+        hi = lo;
+    }
+
+    // Stable compaction in page order: keys above the threshold, then the
+    // first `need` keys equal to it.
+    const uint32_t thr = shr32(prefix, lo);
+    const int per = (n_b + NT - 1) / NT;
+    const int i0 = min(tid * per, n_b), i1 = min(i0 + per, n_b);
+    int cg = 0, ce = 0;
+    for (int i = i0; i < i1; i++) {
+        const uint32_t k = shr32(key_at(i), lo);
+        cg += k > thr;
+        ce += k == thr;
+    }
+    int gb = cg, eb = ce;
+    block_exclusive_scan2<NT>(gb, eb, s_tmp);
+    for (int i = i0; i < i1; i++) {
+        const uint32_t k = shr32(key_at(i), lo);
+        if (k > thr) {
+            const int pos = gb + min(eb, need);
+            if (pos < K) sel[pos] = i;
+            gb++;
+        } else if (k == thr) {
+            if (eb < need && gb + eb < K) sel[gb + eb] = i;
+            eb++;
+        }
+    }
+    if (tid == 0) a.n_selected[row] = K;
+}
+
+// Ticket on the row counter; the last CTA of the row ranks it.
+__device__ __forceinline__ void finish_row(const SelectArgs &a, const RowInfo &r, const float *srow) {
+    __shared__ int s_last;
+    __threadfence();  // this thread's score writes are visible before the ticket
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int t = atomicAdd(&a.tickets[r.row], 1);
+        s_last = (t == int(gridDim.x) - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) a.tickets[r.row] = 0;
+    select_row(a, r.row, r.n_b, srow);
+}
+
+// ---------------------------------------------- scores on tensor cores --
+template <int D, bool QF32>
+__global__ void __launch_bounds__(kSelectThreads) score_select_mma_kernel(SelectArgs a, int score_all) {
+    constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
+    const RowInfo r = row_info(a);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = lane & 3, gid = lane >> 2;
+    float *srow = a.scores + int64_t(r.row) * a.max_pages;
+    const int cta_page0 = blockIdx.x * kSelectThreads;
+
+    if (cta_page0 < r.n_b && (a.top_k < r.n_b || score_all)) {
+        // B operand: the [q- | q+] column of head gid of the group, in the
+        // chunk order this lane uses for the metadata rows.
+        uint32_t bh[NKP][4], bl[NKP][4];
+        const bool head_ok = gid < a.group;
+        const int64_t qoff = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * a.group + (head_ok ? gid : 0)) * D;
+#pragma unroll
+        for (int kp = 0; kp < NKP; kp++) {
+            const int c = 4 * kp + t;
+            const bool upper = 8 * c >= D;  // chunk of the M half: pairs with q+
+            const int col = 8 * c - (upper ? D : 0);
+            float v[8];
+            if (QF32) {
+                const float4 *qp = reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + qoff + col);
+                const float4 x0 = qp[0], x1 = qp[1];
+                v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+                v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+            } else {
+                const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff + col);
+                v[0] = bf16_lo_to_float(x.x); v[1] = bf16_hi_to_float(x.x);
+                v[2] = bf16_lo_to_float(x.y); v[3] = bf16_hi_to_float(x.y);
+                v[4] = bf16_lo_to_float(x.z); v[5] = bf16_hi_to_float(x.z);
+                v[6] = bf16_lo_to_float(x.w); v[7] = bf16_hi_to_float(x.w);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                v[i] = upper ? fmaxf(v[i], 0.f) : fminf(v[i], 0.f);
+                if (!head_ok) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                bh[kp][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                if (QF32) {
+                    const float r0 = v[2 * i] - bf16_lo_to_float(bh[kp][i]);
+                    const float r1 = v[2 * i + 1] - bf16_hi_to_float(bh[kp][i]);
+                    bl[kp][i] = pack_bf16x2(r0, r1);
+                }
+            }
+        }
+
+        const char *meta = static_cast<const char *>(a.meta);
+        const int32_t *trow = a.page_table + int64_t(r.b) * a.max_pages;
+#pragma unroll 1
+        for (int grp = 0; grp < 2; grp++) {
+            const int j0 = cta_page0 + warp * 32 + grp * 16;
+            if (j0 >= r.n_b) break;
+            const int ja = j0 + gid, jb = j0 + gid + 8;
+            const bool va = ja < r.n_b, vb = jb < r.n_b;
+            int pa = va ? trow[ja] : 0, pb = vb ? trow[jb] : 0;
+            const bool bada = va && (pa < 0 || pa >= a.num_pool_pages);
+            const bool badb = vb && (pb < 0 || pb >= a.num_pool_pages);
+            if ((bada || badb) && t == 0) raise_error(a.flags, kErrPageId);
+            uint4 av[NKP], bv[NKP];
+            const char *rowa = meta + (int64_t(pa) * a.num_kv_heads + r.g) * (2 * D * 2);
+            const char *rowb = meta + (int64_t(pb) * a.num_kv_heads + r.g) * (2 * D * 2);
+#pragma unroll
+            for (int kp = 0; kp < NKP; kp++) {
+                const int c = 4 * kp + t;
+                av[kp] = (va && !bada) ? ldg_stream_v4(rowa + c * 16) : make_uint4(0, 0, 0, 0);
+                bv[kp] = (vb && !badb) ? ldg_stream_v4(rowb + c * 16) : make_uint4(0, 0, 0, 0);
+            }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kp = 0; kp < NKP; kp++) {
+                const uint32_t fa0[4] = {av[kp].x, bv[kp].x, av[kp].y, bv[kp].y};
+                const uint32_t fa1[4] = {av[kp].z, bv[kp].z, av[kp].w, bv[kp].w};
+                mma_bf16_16816(acc, fa0, bh[kp][0], bh[kp][1]);
+                mma_bf16_16816(acc, fa1, bh[kp][2], bh[kp][3]);
+                if (QF32) {
+                    mma_bf16_16816(acc, fa0, bl[kp][0], bl[kp][1]);
+                    mma_bf16_16816(acc, fa1, bl[kp][2], bl[kp][3]);
+                }
+            }
+            // acc: [page gid][head 2t], [gid][2t+1], [gid+8][2t], [gid+8][2t+1]
+            const float NEG = -INFINITY;
+            const bool h0 = 2 * t < a.group, h1 = 2 * t + 1 < a.group;
+            float sa = fmaxf(h0 ? acc[0] : NEG, h1 ? acc[1] : NEG);
+            float sb = fmaxf(h0 ? acc[2] : NEG, h1 ? acc[3] : NEG);
+            sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 1));
+            sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 2));
+            sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 1));
+            sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 2));
+            if (t == 0) {
+                if (va) srow[ja] = bada ? NEG : sa;
+                if (vb) srow[jb] = badb ? NEG : sb;
+            }
+        }
+    }
+    finish_row(a, r, srow);
+}
+
+// -------------------------------------------------- scores on CUDA cores --
+template <typename MT, bool QF32>
+__global__ void __launch_bounds__(kSelectThreads) score_select_simt_kernel(SelectArgs a, int D, int score_all) {
+    __shared__ float s_qp[8][128];
+    __shared__ float s_qn[8][128];
+    const RowInfo r = row_info(a);
+    float *srow = a.scores + int64_t(r.row) * a.max_pages;
+    const int j = blockIdx.x * kSelectThreads + threadIdx.x;
+    const bool work = int(blockIdx.x) * kSelectThreads < r.n_b && (a.top_k < r.n_b || score_all);
+    if (work) {
+        for (int e = threadIdx.x; e < a.group * D; e += blockDim.x) {
+            const int h = e / D, c = e % D;
+            const int64_t qi = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * a.group + h) * D + c;
+            const float v = QF32 ? static_cast<const float *>(a.q)[qi]
+                                 : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.q)[qi]);
+            s_qp[h][c] = fmaxf(v, 0.f);
+            s_qn[h][c] = fminf(v, 0.f);
+        }
+    }
+    __syncthreads();
+    if (work && j < r.n_b) {
+        const int p = a.page_table[int64_t(r.b) * a.max_pages + j];
+        if (p < 0 || p >= a.num_pool_pages) {
+            raise_error(a.flags, kErrPageId);
+            srow[j] = -INFINITY;
+        } else {
+            const MT *m = static_cast<const MT *>(a.meta) + (int64_t(p) * a.num_kv_heads + r.g) * 2 * D;
+            const MT *M = m + D;
+            float s[8];
+#pragma unroll
+            for (int h = 0; h < 8; h++) s[h] = 0.f;
+            for (int c = 0; c < D; c++) {
+                const float lo = float(m[c]), hi = float(M[c]);
+#pragma unroll
+                for (int h = 0; h < 8; h++)
+                    if (h < a.group) s[h] = fmaf(s_qp[h][c], hi, fmaf(s_qn[h][c], lo, s[h]));
+            }
+            float best = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < 8; h++)
+                if (h < a.group) best = fmaxf(best, s[h]);
+            srow[j] = best;
+        }
+    }
+    finish_row(a, r, srow);
+}
+
+}  // namespace
+
+cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
+                               int score_all) {
+    const int64_t rows = int64_t(a.batch) * a.num_kv_heads;
+    const dim3 grid(unsigned((a.max_pages + kSelectThreads - 1) / kSelectThreads), unsigned(rows));
+    const dim3 block(kSelectThreads);
+    const bool qf = q_dtype == kDtypeF32;
+    if (meta_dtype == kDtypeBf16) {
+        if (head_dim == 128) {
+            if (qf) score_select_mma_kernel<128, true><<<grid, block, 0, stream>>>(a, score_all);
+            else score_select_mma_kernel<128, false><<<grid, block, 0, stream>>>(a, score_all);
+        } else {
+            if (qf) score_select_mma_kernel<64, true><<<grid, block, 0, stream>>>(a, score_all);
+            else score_select_mma_kernel<64, false><<<grid, block, 0, stream>>>(a, score_all);
+        }
+    } else {
+        if (qf) score_select_simt_kernel<float, true><<<grid, block, 0, stream>>>(a, head_dim, score_all);
+        else score_select_simt_kernel<float, false><<<grid, block, 0, stream>>>(a, head_dim, score_all);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qskv

@@ -1,0 +1,360 @@
+// C ABI of libqskv.so: argument checks, workspace layout, TMA descriptors and
+// kernel launches.  See include/qskv.h for the contract of each call.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "qskv.h"
+#include "qskv_device.cuh"
+#include "qskv_internal.h"
+
+namespace qskv {
+
+DecodeGrid decode_grid(int num_sms) {
+    DecodeGrid g;
+    g.ctas = kDecodeCtasPerSm * num_sms;
+    g.warps_per_cta = kDecodeWarps;
+    g.total_warps = int64_t(g.ctas) * g.warps_per_cta;
+    return g;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms) {
+    WorkspaceLayout w;
+    size_t off = 0;
+    w.flags = off;
+    off += 256;
+    w.sel_tickets = off;
+    off = align256(off + size_t(rows) * 4);
+    w.dec_tickets = off;
+    off = align256(off + size_t(rows) * 4);
+    w.scores = off;
+    off = align256(off + size_t(rows) * size_t(max_pages) * 4);
+    w.slots = rows + decode_grid(num_sms).total_warps;
+    w.part_o = off;
+    off = align256(off + size_t(w.slots) * group * head_dim * 4);
+    w.part_lse = off;
+    off = align256(off + size_t(w.slots) * group * 4);
+    w.total = off;
+    return w;
+}
+
+}  // namespace qskv
+
+using namespace qskv;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qskv_status fail(qskv_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+qskv_status ok() {
+    g_last_error.clear();
+    return QSKV_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// SM count of the current device (cached per device).
+int current_sm_count(int *device_out) {
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (device_out) *device_out = dev;
+    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 128) cache[dev] = n;
+    return n;
+}
+
+qskv_status check_shape(const qskv_shape *s) {
+    if (!s) return fail(QSKV_ERR_INVALID_ARG, "shape is NULL");
+    if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->max_pages < 1 || s->num_pool_pages < 1)
+        return fail(QSKV_ERR_INVALID_ARG, "shape fields must be >= 1 (batch %d, Hq %d, Hkv %d, max_pages %d, pool %d)",
+                    s->batch, s->num_q_heads, s->num_kv_heads, s->max_pages, s->num_pool_pages);
+    if (s->num_q_heads % s->num_kv_heads != 0)
+        return fail(QSKV_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", s->num_q_heads,
+                    s->num_kv_heads);
+    const int G = s->num_q_heads / s->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(QSKV_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", G);
+    if (s->head_dim != 64 && s->head_dim != 128)
+        return fail(QSKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", s->head_dim);
+    if (s->page_size != 16 && s->page_size != 32)
+        return fail(QSKV_ERR_UNSUPPORTED, "page_size must be 16 or 32 (got %d)", s->page_size);
+    const int64_t rows = int64_t(s->batch) * s->num_kv_heads;
+    if (rows > 65535) return fail(QSKV_ERR_UNSUPPORTED, "batch * num_kv_heads must be <= 65535 (got %lld)", (long long)rows);
+    if (int64_t(s->num_pool_pages) >= (int64_t(1) << 25))
+        return fail(QSKV_ERR_UNSUPPORTED, "num_pool_pages must be < 2^25");
+    if (int64_t(s->num_pool_pages) * s->num_kv_heads * s->page_size >= (int64_t(1) << 31))
+        return fail(QSKV_ERR_UNSUPPORTED, "num_pool_pages * num_kv_heads * page_size must be < 2^31");
+    if (int64_t(s->max_pages) * s->page_size >= (int64_t(1) << 31))
+        return fail(QSKV_ERR_UNSUPPORTED, "max_pages * page_size must be < 2^31");
+    return QSKV_OK;
+}
+
+qskv_status check_dtype(int dt, const char *what) {
+    if (dt != QSKV_F32 && dt != QSKV_BF16) return fail(QSKV_ERR_UNSUPPORTED, "%s dtype must be F32 or BF16 (%d)", what, dt);
+    return QSKV_OK;
+}
+
+qskv_status check_workspace(void *ws, size_t bytes, size_t need) {
+    if (!ws) return fail(QSKV_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(QSKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (bytes < need)
+        return fail(QSKV_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, need);
+    return QSKV_OK;
+}
+
+#define QSKV_TRY(expr)                    \
+    do {                                  \
+        qskv_status _s = (expr);          \
+        if (_s != QSKV_OK) return _s;     \
+    } while (0)
+
+// ---------------------------------------------------------- TMA descriptors --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// The pool viewed as a 2-D bf16 tensor [rows = Npool*Hkv*P][D], loaded in
+// boxes of 16 token rows x 64 dims with 128-byte swizzle.
+qskv_status make_pool_map(CUtensorMap *map, const void *pool, const qskv_shape *s) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(QSKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const cuuint64_t dims[2] = {cuuint64_t(s->head_dim),
+                                cuuint64_t(s->num_pool_pages) * s->num_kv_heads * s->page_size};
+    const cuuint64_t strides[1] = {cuuint64_t(s->head_dim) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QSKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return QSKV_OK;
+}
+
+qskv_status launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qskv_workspace_size(const qskv_shape *shape) {
+    if (check_shape(shape) != QSKV_OK) return 0;
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) {
+        fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+        return 0;
+    }
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    return workspace_layout(rows, shape->num_q_heads / shape->num_kv_heads, shape->head_dim, shape->max_pages, sms)
+        .total;
+}
+
+qskv_status qskv_kv_meta_build(const void *k_pool, qskv_dtype kv_dtype, const qskv_shape *shape,
+                               const int32_t *page_ids, const int32_t *valid_tokens, int32_t n_pages, void *meta,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (n_pages < 0) return fail(QSKV_ERR_INVALID_ARG, "n_pages must be >= 0 (got %d)", n_pages);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, 256));
+    if (n_pages == 0) return ok();
+    if (!k_pool || !page_ids || !valid_tokens || !meta)
+        return fail(QSKV_ERR_INVALID_ARG, "k_pool, page_ids, valid_tokens and meta must be non-NULL");
+    if (!aligned(k_pool, 16) || !aligned(meta, 16)) return fail(QSKV_ERR_INVALID_ARG, "k_pool and meta must be 16-byte aligned");
+    if (!aligned(page_ids, 4) || !aligned(valid_tokens, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "page_ids and valid_tokens must be 4-byte aligned");
+    MetaArgs a;
+    a.k_pool = k_pool;
+    a.page_ids = page_ids;
+    a.valid_tokens = valid_tokens;
+    a.meta = meta;
+    a.flags = static_cast<uint32_t *>(workspace);
+    a.n_list = n_pages;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.page_size = shape->page_size;
+    a.num_pool_pages = shape->num_pool_pages;
+    return launched(launch_meta_build(a, kv_dtype, shape->head_dim, static_cast<cudaStream_t>(stream)),
+                    "kv_meta_build launch");
+}
+
+qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta, qskv_dtype meta_dtype,
+                             const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
+                             int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(meta_dtype, "meta"));
+    if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
+    if (!q || !meta || !page_table || !seq_lens || !selected || !n_selected)
+        return fail(QSKV_ERR_INVALID_ARG, "q, meta, page_table, seq_lens, selected and n_selected must be non-NULL");
+    if (!aligned(q, 16) || !aligned(meta, 16)) return fail(QSKV_ERR_INVALID_ARG, "q and meta must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(scores, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and score arrays must be 4-byte aligned");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    SelectArgs a;
+    a.q = q;
+    a.meta = meta;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.scores = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
+    a.tickets = reinterpret_cast<int32_t *>(ws + L.sel_tickets);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = top_k;
+    return launched(launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
+                                       scores != nullptr),
+                    "page_select launch");
+}
+
+qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
+                                     qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                     const qskv_shape *shape, const int32_t *selected, const int32_t *n_selected,
+                                     int32_t top_k, float sm_scale, float *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out)
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool, page_table, seq_lens and out must be non-NULL");
+    if (selected && (!n_selected || top_k < 1))
+        return fail(QSKV_ERR_INVALID_ARG, "with a selected list, n_selected must be non-NULL and top_k >= 1");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool and out must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(lse, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and lse arrays must be 4-byte aligned");
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return fail(QSKV_ERR_INVALID_ARG, "sm_scale must be finite and >= 0");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    const DecodeGrid grid = decode_grid(sms);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+
+    DecodeArgs a;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float *>(ws + L.part_o);
+    a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    a.tickets = reinterpret_cast<int32_t *>(ws + L.dec_tickets);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = selected ? top_k : 0;
+    a.slots_per_row = selected ? top_k : shape->max_pages;
+    a.stages = decode_stages(shape->head_dim);
+    a.total_units = rows * a.slots_per_row;
+    a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
+    const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    if (kv_dtype == QSKV_BF16) {
+        QSKV_TRY(make_pool_map(&tk, k_pool, shape));
+        QSKV_TRY(make_pool_map(&tv, v_pool, shape));
+    }
+    return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, static_cast<cudaStream_t>(stream)),
+                    "sparse_paged_decode launch");
+}
+
+qskv_status qskv_get_error(void *workspace, void *stream) {
+    if (!workspace) return fail(QSKV_ERR_WORKSPACE, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t flags = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof flags, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "qskv_get_error: %s", cudaGetErrorString(e));
+    if (flags == 0) return ok();
+    std::string what;
+    if (flags & kErrPageId) what += " page-id-out-of-range";
+    if (flags & kErrSelected) what += " selected-index-out-of-range";
+    if (flags & kErrSeqLen) what += " seq_len-out-of-range";
+    if (flags & kErrValid) what += " valid-tokens-out-of-range";
+    if (flags & kErrTimeout) what += " wait-timeout";
+    if (flags & kErrTimeout) return fail(QSKV_ERR_DEVICE_TIMEOUT, "device flags:%s", what.c_str());
+    return fail(QSKV_ERR_DEVICE_INDEX, "device flags:%s", what.c_str());
+}
+
+const char *qskv_status_string(qskv_status status) {
+    switch (status) {
+        case QSKV_OK: return "QSKV_OK";
+        case QSKV_ERR_INVALID_ARG: return "QSKV_ERR_INVALID_ARG";
+        case QSKV_ERR_UNSUPPORTED: return "QSKV_ERR_UNSUPPORTED";
+        case QSKV_ERR_WORKSPACE: return "QSKV_ERR_WORKSPACE";
+        case QSKV_ERR_CUDA: return "QSKV_ERR_CUDA";
+        case QSKV_ERR_DEVICE_INDEX: return "QSKV_ERR_DEVICE_INDEX";
+        case QSKV_ERR_DEVICE_TIMEOUT: return "QSKV_ERR_DEVICE_TIMEOUT";
+    }
+    return "QSKV_UNKNOWN_STATUS";
+}
+
+const char *qskv_last_error_message(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// Host-side declarations shared by the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qskv {
+
+constexpr int kDtypeF32 = 0;  // matches QSKV_F32
+constexpr int kDtypeBf16 = 1; // matches QSKV_BF16
+
+struct MetaArgs;
+struct SelectArgs;
+struct DecodeArgs;
+
+// Workspace layout: every region starts on a 256-byte boundary.
+struct WorkspaceLayout {
+    size_t flags;        // uint32 error word (+ padding to 256 B)
+    size_t sel_tickets;  // int32 [rows]
+    size_t dec_tickets;  // int32 [rows]
+    size_t scores;       // fp32  [rows][max_pages]
+    size_t part_o;       // fp32  [slots][G][D]
+    size_t part_lse;     // fp32  [slots][G]
+    size_t total;
+    int64_t slots;       // rows + decode warps
+};
+
+// Decode grid shape on a device with `num_sms` SMs.
+struct DecodeGrid {
+    int ctas;
+    int warps_per_cta;
+    int64_t total_warps;
+};
+
+DecodeGrid decode_grid(int num_sms);
+WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms);
+
+cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream);
+// score_all: compute scores even for rows where every page is kept.
+cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
+                               int score_all);
+// tmap_k / tmap_v are used by the bf16 tensor-core kernel only.
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
+                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream);
+// Stage count and dynamic shared memory of the bf16 decode kernel.
+int decode_stages(int head_dim);
+size_t decode_smem_bytes(int head_dim, int stages);
+
+}  // namespace qskv

@@ -1,0 +1,81 @@
+"""Buffer plumbing around the three C-ABI calls for one paged KV cache.
+
+``PagedDecoder`` owns the device buffers a decode step needs (metadata,
+workspace, selection, outputs) and issues the calls in order.  It only
+allocates and passes pointers; every step of the computation runs in
+libqskv.so's kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class PagedDecoder:
+    """One decode batch over a paged KV cache resident on the GPU.
+
+    q           [batch][Hq][d]            fp32 or bf16
+    k_pool      [Npool][Hkv][P][d]        fp32 or bf16 (v_pool the same)
+    page_table  [batch][max_pages] int32  physical page ids
+    seq_lens    [batch] int32
+    top_k       pages kept per (sequence, KV head); None = dense decode
+    """
+
+    def __init__(self, q, k_pool, v_pool, page_table, seq_lens, top_k: Optional[int], sm_scale: float = 0.0):
+        dev = k_pool.device
+        self.q, self.k_pool, self.v_pool = q, k_pool, v_pool
+        self.page_table, self.seq_lens = page_table, seq_lens
+        n_pool, hkv, P, d = k_pool.shape
+        batch, hq, _ = q.shape
+        self.top_k = top_k
+        self.sm_scale = sm_scale
+        self.shape = B.make_shape(batch, hq, hkv, d, P, page_table.shape[1], n_pool)
+        self.meta = torch.empty((n_pool, hkv, 2, d), dtype=k_pool.dtype, device=dev)
+        self.workspace = torch.zeros(B.workspace_size(self.shape), dtype=torch.uint8, device=dev)
+        k = max(int(top_k or 1), 1)
+        self.selected = torch.full((batch, hkv, k), -1, dtype=torch.int32, device=dev)
+        self.n_selected = torch.zeros((batch, hkv), dtype=torch.int32, device=dev)
+        self.out = torch.empty((batch, hq, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((batch, hq), dtype=torch.float32, device=dev)
+
+    # -- cache phase ---------------------------------------------------------
+    def build_meta(self, page_ids: torch.Tensor, valid_tokens: torch.Tensor, stream=None):
+        B.kv_meta_build(self.k_pool, page_ids, valid_tokens, self.meta, self.shape, self.workspace, stream)
+
+    # -- indexer phase -------------------------------------------------------
+    def select(self, q=None, scores: Optional[torch.Tensor] = None, stream=None):
+        B.page_select(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k,
+                      self.selected, self.n_selected, self.shape, self.workspace, scores, stream)
+
+    def decode(self, q=None, dense: bool = False, out=None, lse=None, stream=None):
+        sel = None if (dense or self.top_k is None) else self.selected
+        B.sparse_paged_decode(self.q if q is None else q, self.k_pool, self.v_pool, self.page_table, self.seq_lens,
+                              self.out if out is None else out, self.shape, self.workspace, selected=sel,
+                              n_selected=self.n_selected if sel is not None else None,
+                              top_k=self.top_k or 0, lse=self.lse if lse is None else lse, sm_scale=self.sm_scale,
+                              stream=stream)
+
+    def step(self, q=None, last_ids=None, last_valid=None, stream=None):
+        """Metadata refresh of the pages being appended to, selection, decode."""
+        if last_ids is not None:
+            self.build_meta(last_ids, last_valid, stream)
+        if self.top_k is not None:
+            self.select(q, stream=stream)
+        self.decode(q, stream=stream)
+
+    def check(self, stream=None):
+        """Raise if the device flagged an out-of-range index or a timeout."""
+        st = B.get_error(self.workspace, stream)
+        if st != 0:
+            raise B.QskvError(st, B.last_error_message())
+
+
+def from_inputs(inputs: dict, device="cuda", top_k="spec") -> PagedDecoder:
+    """A PagedDecoder over a workloads.make_inputs() batch copied to `device`."""
+    if isinstance(top_k, str):
+        top_k = inputs["top_k"]
+    t = {k: inputs[k].to(device) for k in ("q", "k_pool", "v_pool", "page_table", "seq_lens")}
+    return PagedDecoder(t["q"], t["k_pool"], t["v_pool"], t["page_table"], t["seq_lens"], top_k)
