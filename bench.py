@@ -241,8 +241,9 @@ def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_targ
         if step_target_s is not None:
             break
     steps_per_s = (done_rows / n_rows) / t_total
-    sample = (f"{done_rows} of {n_rows} (sequence, KV head) rows per full step, full step = "
-              f"scores + top-K + attention; {cores} OpenMP threads; {t_total:.2f} s")
+    sample = (f"{steps} samples of {n} random rows out of the {n_rows} (sequence, KV head) rows of a step "
+              f"(scores + top-K + attention per row), {done_rows / n_rows:.2f} full steps in {t_total:.2f} s "
+              f"on {cores} OpenMP threads")
     return steps_per_s, cores, sample, n
 
 

@@ -1,0 +1,41 @@
+"""The benchmark's algorithmic byte counts against hand-worked sizes."""
+import numpy as np
+import torch
+
+import bench
+from query_aware_sparse_kv_gb300 import workloads as W
+
+
+def test_tiny_step_bytes():
+    """tiny: 2 sequences x 2 KV heads, 16 full pages of 16 tokens, d=64,
+    fp32, top-4.  decode reads 4 rows x 4 pages x (16 x 64 x 4 B) x (K, V)
+    = 131072 B of KV; select reads 4 rows x 16 pages x 2 x 64 x 4 B = 32768 B
+    of metadata."""
+    inp = W.make_inputs(W.spec_for("tiny"))
+    sel = np.tile(np.arange(4, dtype=np.int32), (2, 2, 1))
+    nsel = np.full((2, 2), 4, dtype=np.int32)
+    nb = bench.step_bytes(inp, sel, nsel)
+    assert nb["kv"] == 4 * 4 * 16 * 64 * 4 * 2
+    q = 2 * 4 * 64 * 4
+    out = 2 * 4 * 64 * 4 + 2 * 4 * 4
+    selb = 2 * 2 * 4 * 4 + 2 * 2 * 4
+    assert nb["decode"] == nb["kv"] + q + out + selb + 16 * 4
+    assert nb["select"] == 4 * 16 * (2 * 64 * 4 + 4 + 8) + q + selb
+    assert nb["meta"] == 2 * 2 * (16 * 64 * 4 + 2 * 64 * 4)
+
+
+def test_partial_last_page_counts_only_loaded_subtiles():
+    """A 32-token page with 5 valid tokens is read as one 16-token sub-tile."""
+    spec = W.Spec(name="p", batch=1, num_q_heads=2, num_kv_heads=1, head_dim=128, page_size=32, seq_lens=(37,),
+                  top_k=2, kind="iid")
+    inp = W.make_inputs(spec)
+    nb = bench.step_bytes(inp, np.array([[[0, 1]]]), np.array([[2]]))
+    assert nb["kv"] == (2 + 1) * 16 * 128 * 2 * 2
+
+
+def test_dense_counts_every_page():
+    spec = W.spec_for("shared_prefix", batch=3, prefix_pages=2, suffix_pages=1)
+    inp = W.make_inputs(spec)
+    nb = bench.step_bytes(inp, None, None)
+    assert nb["kv"] == 3 * 8 * 3 * 16 * 128 * 2 * 2
+    assert nb["select"] == 0
