@@ -330,7 +330,11 @@ def run_gpu(args):
     barrier(world)
     qskv.load()
 
-    spec = shard_spec(W.spec_for(args.workload), rank)
+    spec = W.spec_for(args.workload)
+    if args.batch:
+        spec = W.spec_for(args.workload, batch=args.batch,
+                          seq_lens=spec.seq_lens[:1] * args.batch if spec.seq_lens else None)
+    spec = shard_spec(spec, rank)
     inputs = W.make_inputs(spec)
     qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
     dec = qskv.from_inputs(inputs, device=dev)
@@ -401,7 +405,7 @@ def run_gpu(args):
     value = world * args.steps / (elapsed_ms / 1000.0)
 
     # end to end through the public API: pinned host q in, host out back, every step
-    e2e_steps = min(args.steps, 500)
+    e2e_steps = 0 if args.no_e2e else min(args.steps, 500)
     q_host = qv_cpu.pin_memory()
     q_dev = torch.empty_like(qv[0])
     out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
@@ -418,7 +422,7 @@ def run_gpu(args):
         torch.cuda.current_stream().synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     dec.check()
-    e2e_value = world * e2e_steps / e2e_s
+    e2e_value = world * e2e_steps / e2e_s if e2e_steps else None
 
     if rank != 0:
         return 0
@@ -467,6 +471,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
