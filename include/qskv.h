@@ -161,6 +161,34 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
                                      size_t workspace_bytes, void *stream);
 
 /*
+ * qskv_sparse_paged_decode without a workspace, for callers that cannot
+ * allocate device memory: for example a serving engine whose memory planner
+ * hands out every byte of HBM up front and forbids later cudaMalloc calls,
+ * or a latency-critical decode loop where cudaMalloc (which may synchronise
+ * the device) is not allowed.  The pages have no counterpart of this call.
+ *
+ * Same arguments and results as qskv_sparse_paged_decode minus the
+ * workspace.  The split partials, row counters and error word live in an
+ * 8 MiB array of device memory built into the library (every GPU that loads
+ * the library holds it until the process exits).  A shape whose scratch
+ * (256 B + 4 B per row + (rows + 8 x SM count) x G x (head_dim + 1) x 4 B)
+ * exceeds 8 MiB is rejected with QSKV_ERR_WORKSPACE before any launch.
+ * Each call clears the error word and the counters with cudaMemsetAsync on
+ * `stream`; nothing is allocated or freed.  Device-side index errors still
+ * skip the offending page but are not reported (no workspace to read them
+ * from): use qskv_sparse_paged_decode to diagnose.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array: calls that may overlap on the GPU (other streams,
+ * other host threads) race and corrupt each other's results.
+ */
+qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, const void *k_pool,
+                                             const void *v_pool, qskv_dtype kv_dtype, const int32_t *page_table,
+                                             const int32_t *seq_lens, const qskv_shape *shape,
+                                             const int32_t *selected, const int32_t *n_selected, int32_t top_k,
+                                             float sm_scale, float *out, float *lse, void *stream);
+
+/*
  * Synchronises `stream`, reads and clears the workspace's device error flags,
  * and returns QSKV_OK, QSKV_ERR_DEVICE_INDEX, QSKV_ERR_DEVICE_TIMEOUT or
  * QSKV_ERR_CUDA.  The only call that blocks the host.

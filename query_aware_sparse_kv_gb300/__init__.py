@@ -12,9 +12,11 @@ plus ``PagedDecoder`` (buffer plumbing for a whole step) and ``workloads``
 built library every call raises.
 """
 from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, get_error, kv_meta_build,
-                      last_error_message, load, make_shape, page_select, sparse_paged_decode, workspace_size)
+                      last_error_message, load, make_shape, page_select, sparse_paged_decode,
+                      sparse_paged_decode_noalloc, workspace_size)
 from .engine import PagedDecoder, from_inputs
 
 __all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "get_error", "kv_meta_build",
-           "last_error_message", "load", "make_shape", "page_select", "sparse_paged_decode", "workspace_size",
+           "last_error_message", "load", "make_shape", "page_select", "sparse_paged_decode",
+           "sparse_paged_decode_noalloc", "workspace_size",
            "PagedDecoder", "from_inputs"]

@@ -23,7 +23,7 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
 
 # Every function the header declares, in declaration order.
 EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_sparse_paged_decode",
-           "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
+           "qskv_sparse_paged_decode_noalloc", "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
 
 
 class QskvLibraryMissing(RuntimeError):
@@ -68,6 +68,9 @@ def load(path: str = LIB_PATH):
     lib.qskv_sparse_paged_decode.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p, i32p, i32,
                                              ctypes.c_float, f32p, f32p, vp, sz, vp]
+    lib.qskv_sparse_paged_decode_noalloc.restype = ctypes.c_int
+    lib.qskv_sparse_paged_decode_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p,
+                                                     i32p, i32, ctypes.c_float, f32p, f32p, vp]
     lib.qskv_get_error.restype = ctypes.c_int
     lib.qskv_get_error.argtypes = [vp, vp]
     lib.qskv_status_string.restype = ctypes.c_char_p
@@ -141,6 +144,22 @@ def sparse_paged_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Ten
                                            _ptr(n_selected), int(top_k), float(sm_scale), _ptr(out), _ptr(lse),
                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                                            _stream(stream)))
+
+
+def sparse_paged_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                page_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, shape: Shape,
+                                selected: Optional[torch.Tensor] = None, n_selected: Optional[torch.Tensor] = None,
+                                top_k: int = 0, lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
+                                stream=None):
+    """sparse_paged_decode for callers that cannot allocate device memory
+    (their memory planner owns all of HBM, or their decode loop must not
+    call the allocator).  The library's built-in 8 MiB scratch replaces the
+    workspace; this wrapper allocates nothing either.  Calls that may overlap
+    on the GPU share that scratch and race."""
+    _check(load().qskv_sparse_paged_decode_noalloc(_ptr(q), _dtype(q), _ptr(k_pool), _ptr(v_pool), _dtype(k_pool),
+                                                   _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape),
+                                                   _ptr(selected), _ptr(n_selected), int(top_k), float(sm_scale),
+                                                   _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def get_error(workspace: torch.Tensor, stream=None) -> int:

@@ -37,6 +37,8 @@
 // the P.V product and the same rounded values feed the softmax denominator.
 //
 // fp32 KV runs a CUDA-core kernel with the same decomposition and merge.
+#include <mutex>
+
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
 
@@ -539,6 +541,31 @@ cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtens
 }
 
 }  // namespace
+
+// Scratch of qskv_sparse_paged_decode_noalloc: the error word, the per-row
+// merge counters and the split partial outputs live here instead of in a
+// caller-allocated workspace.  Every device that loads the library holds
+// these bytes until the process exits.  All calls share them.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+cudaError_t noalloc_scratch_address(void **ptr) {
+    // Resolved once per device, with that device current.
+    static void *addr[64] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
 
 int decode_stages(int head_dim) { return head_dim == 128 ? 3 : 6; }
 

@@ -322,6 +322,90 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
                     "sparse_paged_decode launch");
 }
 
+qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, const void *k_pool,
+                                             const void *v_pool, qskv_dtype kv_dtype, const int32_t *page_table,
+                                             const int32_t *seq_lens, const qskv_shape *shape,
+                                             const int32_t *selected, const int32_t *n_selected, int32_t top_k,
+                                             float sm_scale, float *out, float *lse, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out)
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool, page_table, seq_lens and out must be non-NULL");
+    if (selected && (!n_selected || top_k < 1))
+        return fail(QSKV_ERR_INVALID_ARG, "with a selected list, n_selected must be non-NULL and top_k >= 1");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool and out must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(lse, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and lse arrays must be 4-byte aligned");
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return fail(QSKV_ERR_INVALID_ARG, "sm_scale must be finite and >= 0");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const DecodeGrid grid = decode_grid(sms);
+
+    // Layout inside the static scratch: error word, row counters, partials.
+    const int64_t slots = rows + grid.total_warps;
+    const size_t off_tickets = 256;
+    const size_t off_part_o = align256(off_tickets + size_t(rows) * 4);
+    const size_t off_part_lse = align256(off_part_o + size_t(slots) * G * shape->head_dim * 4);
+    const size_t need = align256(off_part_lse + size_t(slots) * G * 4);
+    if (need > kNoallocScratchBytes)
+        return fail(QSKV_ERR_WORKSPACE,
+                    "this shape needs %zu bytes of decode scratch but the built-in buffer holds %zu; "
+                    "call qskv_sparse_paged_decode with a caller-allocated workspace instead",
+                    need, kNoallocScratchBytes);
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "cudaGetSymbolAddress of the decode scratch: %s", cudaGetErrorString(e));
+    uint8_t *ws = static_cast<uint8_t *>(scratch);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the error word and the row counters must start at zero on every call
+    e = cudaMemsetAsync(ws, 0, off_part_o, st);
+    if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "clearing the decode scratch: %s", cudaGetErrorString(e));
+
+    DecodeArgs a;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float *>(ws + off_part_o);
+    a.part_lse = reinterpret_cast<float *>(ws + off_part_lse);
+    a.tickets = reinterpret_cast<int32_t *>(ws + off_tickets);
+    a.flags = reinterpret_cast<uint32_t *>(ws);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = selected ? top_k : 0;
+    a.slots_per_row = selected ? top_k : shape->max_pages;
+    a.stages = decode_stages(shape->head_dim);
+    a.total_units = rows * a.slots_per_row;
+    a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
+    const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    if (kv_dtype == QSKV_BF16) {
+        QSKV_TRY(make_pool_map(&tk, k_pool, shape));
+        QSKV_TRY(make_pool_map(&tv, v_pool, shape));
+    }
+    return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, st),
+                    "sparse_paged_decode_noalloc launch");
+}
+
 qskv_status qskv_get_error(void *workspace, void *stream) {
     if (!workspace) return fail(QSKV_ERR_WORKSPACE, "workspace is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -44,6 +44,11 @@ cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype,
 // tmap_k / tmap_v are used by the bf16 tensor-core kernel only.
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
                           int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream);
+// Size of the static device scratch used by qskv_sparse_paged_decode_noalloc
+// and its device address on the current device (looked up on first use).
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
+cudaError_t noalloc_scratch_address(void **ptr);
+
 // Stage count and dynamic shared memory of the bf16 decode kernel.
 int decode_stages(int head_dim);
 size_t decode_smem_bytes(int head_dim, int stages);
