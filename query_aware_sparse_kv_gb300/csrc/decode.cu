@@ -47,44 +47,51 @@ namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-// (physical page << 6 | valid tokens) of unit u, or -1 when the unit is
-// empty or names an out-of-range page (flagged).
-__device__ __forceinline__ int unit_code(const DecodeArgs &a, int64_t u, int64_t u_end) {
-    if (u >= u_end) return -1;
-    const int row = int(u / a.slots_per_row);
-    const int slot = int(u % a.slots_per_row);
+// (physical page << 6 | valid tokens) of slot `slot` of row `row`, or -1
+// when the slot is empty or names an out-of-range page (flagged).  The
+// index loads that do not depend on each other are issued together.
+__device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot) {
     const int b = row / a.num_kv_heads;
-    int seq = a.seq_lens[b];
+    int seq = __ldg(a.seq_lens + b);
+    int ns = 0, j = slot;
+    if (a.selected) {
+        ns = __ldg(a.n_selected + row);
+        j = __ldg(a.selected + int64_t(row) * a.top_k + slot);
+    }
     const int cap = a.max_pages * a.page_size;
     if (seq < 0 || seq > cap) {
         raise_error(a.flags, kErrSeqLen);
         seq = seq < 0 ? 0 : cap;
     }
     const int n_b = (seq + a.page_size - 1) / a.page_size;
-    int j;
     if (a.selected) {
-        int ns = a.n_selected[row];
         const int lim = min(a.top_k, n_b);
         if (ns < 0 || ns > lim) {
             raise_error(a.flags, kErrSelected);
             ns = max(0, min(ns, lim));
         }
         if (slot >= ns) return -1;
-        j = a.selected[int64_t(row) * a.top_k + slot];
         if (j < 0 || j >= n_b) {
             raise_error(a.flags, kErrSelected);
             return -1;
         }
-    } else {
-        if (slot >= n_b) return -1;
-        j = slot;
+    } else if (slot >= n_b) {
+        return -1;
     }
-    const int p = a.page_table[int64_t(b) * a.max_pages + j];
+    const int p = __ldg(a.page_table + int64_t(b) * a.max_pages + j);
     if (p < 0 || p >= a.num_pool_pages) {
         raise_error(a.flags, kErrPageId);
         return -1;
     }
     return (p << 6) | min(a.page_size, seq - j * a.page_size);
+}
+
+// Code of unit (row, slot) + lane offset `k` (0 <= k < 64), -1 past u_end.
+__device__ __forceinline__ int unit_code_at(const DecodeArgs &a, int row, int slot, int k, int64_t u, int64_t u_end) {
+    if (u + k >= u_end) return -1;
+    const int s = slot + k;
+    const int dr = s / a.slots_per_row;
+    return unit_code(a, row + dr, s - dr * a.slots_per_row);
 }
 
 // Warps whose unit ranges intersect row `row`.
@@ -95,35 +102,80 @@ __device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t 
     w1 = last / a.units_per_warp;
 }
 
-// One warp merges the partials of row `row` from warps w0..w1 (slots row+w).
+// One warp merges the partials of row `row` from warps w0..w1 (slots row+w):
+// out = sum_s 2^(lse_s - max) o_s / sum_s 2^(lse_s - max), in one pass with
+// a running maximum.  Each lane owns up to four float4 positions of the
+// row's G x D output and loads four slots' partials for all of them at once,
+// so a merge costs a few L2 round trips whatever the number of slots.
 template <int D>
 __device__ void merge_row(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
+    constexpr int V4 = D / 4;
+    constexpr int IT = 4;  // float4 positions per lane per pass
+    constexpr int SC = 4;  // slots per batch of loads
     const int lane = threadIdx.x & 31;
     const int G = a.group;
     const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
-    constexpr int V4 = D / 4;
-    for (int idx = lane; idx < G * V4; idx += 32) {
-        const int h = idx / V4, c4 = idx % V4;
-        float mx = -INFINITY;
-        for (int64_t w = w0; w <= w1; w++) mx = fmaxf(mx, __ldcg(a.part_lse + (row + w) * G + h));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.f;
-        if (mx != -INFINITY) {
-            for (int64_t w = w0; w <= w1; w++) {
-                const int64_t slot = row + w;
-                const float wt = exp2f(__ldcg(a.part_lse + slot * G + h) - mx);
-                const float4 o = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (slot * G + h) * D) + c4);
-                den += wt;
-                acc.x = fmaf(wt, o.x, acc.x);
-                acc.y = fmaf(wt, o.y, acc.y);
-                acc.z = fmaf(wt, o.z, acc.z);
-                acc.w = fmaf(wt, o.w, acc.w);
+    const int ns = int(w1 - w0 + 1);
+    const int n_items = G * V4;
+    const float *lse_base = a.part_lse + (row + w0) * G;
+    const float4 *o_base = reinterpret_cast<const float4 *>(a.part_o) + (row + w0) * G * V4;
+    const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+    for (int i0 = 0; i0 < n_items; i0 += 32 * IT) {
+        float mx[IT], den[IT];
+        float4 acc[IT];
+#pragma unroll
+        for (int k = 0; k < IT; k++) {
+            mx[k] = -INFINITY;
+            den[k] = 0.f;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int s0 = 0; s0 < ns; s0 += SC) {
+            float l[SC][IT];
+            float4 v[SC][IT];
+#pragma unroll
+            for (int j = 0; j < SC; j++) {
+#pragma unroll
+                for (int k = 0; k < IT; k++) {
+                    const int it = i0 + lane + 32 * k;
+                    const bool ok = it < n_items && s0 + j < ns;
+                    l[j][k] = ok ? __ldcg(lse_base + (s0 + j) * G + it / V4) : -INFINITY;
+                    v[j][k] = ok ? __ldcg(o_base + (s0 + j) * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < IT; k++) {
+                float m = mx[k];
+#pragma unroll
+                for (int j = 0; j < SC; j++) m = fmaxf(m, l[j][k]);
+                if (m == -INFINITY) continue;
+                const float sc = exp2f(mx[k] - m);
+                den[k] *= sc;
+                acc[k].x *= sc;
+                acc[k].y *= sc;
+                acc[k].z *= sc;
+                acc[k].w *= sc;
+#pragma unroll
+                for (int j = 0; j < SC; j++) {
+                    const float w = exp2f(l[j][k] - m);
+                    den[k] += w;
+                    acc[k].x = fmaf(w, v[j][k].x, acc[k].x);
+                    acc[k].y = fmaf(w, v[j][k].y, acc[k].y);
+                    acc[k].z = fmaf(w, v[j][k].z, acc[k].z);
+                    acc[k].w = fmaf(w, v[j][k].w, acc[k].w);
+                }
+                mx[k] = m;
             }
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G + h;
-        reinterpret_cast<float4 *>(a.out + qh * D)[c4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (c4 == 0 && a.lse) a.lse[qh] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < IT; k++) {
+            const int it = i0 + lane + 32 * k;
+            if (it >= n_items) continue;
+            const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;
+            const int h = it / V4, c4 = it % V4;
+            reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
+                make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+            if (c4 == 0 && a.lse) a.lse[qh0 + h] = den[k] > 0.f ? (mx[k] + log2f(den[k])) * kLn2 : -INFINITY;
+        }
     }
 }
 
@@ -142,6 +194,37 @@ __device__ __forceinline__ void arrive_row(const DecodeArgs &a, int row, int64_t
         merge_row<D>(a, row, w0, w1);
         if (lane == 0) a.tickets[row] = 0;
     }
+}
+
+// Deferred arrivals: lane i of the warp holds the i-th row whose partial this
+// warp wrote and has not yet reported (-1 for none).  Reporting them all at
+// once -- one fence, one ticket per row in parallel lanes, then the merges
+// this warp completes -- keeps those round trips out of the streaming loop.
+template <int D>
+__device__ __forceinline__ void arrive_deferred(const DecodeArgs &a, int &drow, int &dcount) {
+    if (dcount == 0) return;
+    const int lane = threadIdx.x & 31;
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane < dcount) {
+        int64_t w0, w1;
+        row_warps(a, drow, w0, w1);
+        last = atomicAdd(a.tickets + drow, 1) == int(w1 - w0);
+    }
+    unsigned mask = __ballot_sync(0xffffffffu, last);
+    if (mask) __threadfence();
+    while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int r = __shfl_sync(0xffffffffu, drow, i);
+        int64_t w0, w1;
+        row_warps(a, r, w0, w1);
+        merge_row<D>(a, r, w0, w1);
+        if (lane == 0) a.tickets[r] = 0;
+    }
+    drow = -1;
+    dcount = 0;
 }
 
 // ------------------------------------------------- bf16 KV, tensor cores --
@@ -178,10 +261,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     }
     __syncwarp();
 
-    // Codes of units [wbase, wbase + 64): lane i holds units wbase+i and wbase+32+i.
+    // Units are walked with (row, slot) cursors, never by dividing the
+    // 64-bit unit index in the loop.
+    const int spr = a.slots_per_row;
+    const int row_begin = int(u_begin / spr);
+    const int slot_begin = int(u_begin - int64_t(row_begin) * spr);
+
+    // Codes of units [wbase, wbase + 64): lane i holds units wbase+i and
+    // wbase+32+i; (wrow, wslot) are the coordinates of wbase.
     int64_t wbase = u_begin;
-    int code_cur = unit_code(a, wbase + lane, u_end);
-    int code_nxt = unit_code(a, wbase + 32 + lane, u_end);
+    int wrow = row_begin, wslot = slot_begin;
+    int code_cur = unit_code_at(a, wrow, wslot, lane, wbase, u_end);
+    int code_nxt = unit_code_at(a, wrow, wslot, 32 + lane, wbase, u_end);
     auto code_of = [&](int64_t u) -> int {
         const int k = int(u - wbase);
         const int c0 = __shfl_sync(0xffffffffu, code_cur, k & 31);
@@ -191,34 +282,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
 
     // ---------------- producer: lane 0 issues TMA for the next sub-tiles
     int64_t pu = u_begin;
+    int pslot = slot_begin, pg = row_begin % a.num_kv_heads;
     int psub = 0, ps = 0;
     uint32_t issued = 0, consumed = 0;
     auto produce = [&]() {
         while (int(issued - consumed) < S && pu < u_end && pu - wbase < 64) {
             const int code = code_of(pu);
-            if (code < 0) {
-                pu++;
-                psub = 0;
-                continue;
-            }
-            const int valid = code & 63, phys = code >> 6;
-            const int g = int(pu / a.slots_per_row) % a.num_kv_heads;
-            if (lane == 0) {
-                uint8_t *st = ring + size_t(ps) * STAGE;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar + ps, STAGE);
-                const int y = (phys * a.num_kv_heads + g) * a.page_size + psub * 16;
+            int nsub = 0;
+            if (code >= 0) {
+                const int valid = code & 63, phys = code >> 6;
+                nsub = (valid + 15) >> 4;
+                if (lane == 0) {
+                    uint8_t *st = ring + size_t(ps) * STAGE;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar + ps, STAGE);
+                    const int y = (phys * a.num_kv_heads + pg) * a.page_size + psub * 16;
 #pragma unroll
-                for (int nb = 0; nb < NB; nb++) {
-                    tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y, bar + ps);
-                    tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y, bar + ps);
+                    for (int nb = 0; nb < NB; nb++) {
+                        tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y, bar + ps);
+                        tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y, bar + ps);
+                    }
                 }
+                issued++;
+                ps = ps + 1 == S ? 0 : ps + 1;
             }
-            issued++;
-            ps = ps + 1 == S ? 0 : ps + 1;
-            if (++psub == (valid + 15) >> 4) {
-                pu++;
+            if (++psub >= nsub) {  // next unit
                 psub = 0;
+                pu++;
+                if (++pslot == spr) {
+                    pslot = 0;
+                    if (++pg == a.num_kv_heads) pg = 0;
+                }
             }
         }
     };
@@ -257,6 +351,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         }
     };
 
+    int drow = -1, dcount = 0;  // rows whose partial awaits its ticket (lane i: i-th)
     auto finish_row = [&](int row) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -300,32 +395,45 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 dst[h1 * ldh + d0 + 8] = o[mt][3] * i1;
             }
         }
-        if (w0 != w1) arrive_row<D>(a, row, w0, w1);
+        if (w0 != w1) {
+            if (dcount == 32) arrive_deferred<D>(a, drow, dcount);
+            if (lane == dcount) drow = row;
+            dcount++;
+        }
     };
 
     // ---------------- main loop
     int64_t cu = u_begin;
+    int crow = row_begin, cslot = slot_begin;
     int csub = 0, cs = 0;
     uint32_t cphase = 0;
     bool aborted = false;
     produce();
     while (cu < u_end) {
-        if (cu - wbase >= 32) {
+        if (cu - wbase >= 32) {  // slide the code window by 32 units
             wbase += 32;
+            wslot += 32;
+            while (wslot >= spr) {
+                wslot -= spr;
+                wrow++;
+            }
             code_cur = code_nxt;
-            code_nxt = unit_code(a, wbase + 32 + lane, u_end);
+            code_nxt = unit_code_at(a, wrow, wslot, 32 + lane, wbase, u_end);
         }
         produce();
-        const int row = int(cu / a.slots_per_row);
-        if (row != cur_row) {
+        if (crow != cur_row) {
             if (cur_row >= 0) finish_row(cur_row);
-            cur_row = row;
-            start_row(row);
+            cur_row = crow;
+            start_row(crow);
         }
         const int code = code_of(cu);
         if (code < 0) {
             cu++;
             csub = 0;
+            if (++cslot == spr) {
+                cslot = 0;
+                crow++;
+            }
             continue;
         }
         const int valid = code & 63;
@@ -347,9 +455,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         }
         const uint32_t kb = smem_u32(st), vb = kb + KVB;
 
-        // S^T = K . Q^T
-        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K . Q^T, as two independent accumulation chains
+        float sacc[4];
         {
+            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             const int mat = lane >> 3;
             const int r = (lane & 7) + ((mat & 1) << 3);
 #pragma unroll
@@ -357,9 +466,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 const int c = (ks & 3) * 2 + (mat >> 1);
                 uint32_t af[4];
                 ldmatrix_x4(af, kb + (ks >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
-                mma_bf16_16816(sacc, af, qb[ks][0], qb[ks][1]);
-                if (QF32) mma_bf16_16816(sacc, af, ql[ks][0], ql[ks][1]);
+                mma_bf16_16816(sa[ks & 1], af, qb[ks][0], qb[ks][1]);
+                if (QF32) mma_bf16_16816(sa[ks & 1], af, ql[ks][0], ql[ks][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; i++) sacc[i] = sa[0][i] + sa[1][i];
         }
         // online softmax; sacc = [tok gid][h0], [gid][h1], [gid+8][h0], [gid+8][h1]
         const float sc = a.scale_log2;
@@ -410,6 +521,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         if (++csub == (valid + 15) >> 4) {
             cu++;
             csub = 0;
+            if (++cslot == spr) {
+                cslot = 0;
+                crow++;
+            }
         }
     }
     if (aborted) {
@@ -425,6 +540,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         return;
     }
     if (cur_row >= 0) finish_row(cur_row);
+    arrive_deferred<D>(a, drow, dcount);
 }
 
 // --------------------------------------------------- fp32 KV, CUDA cores --
@@ -488,7 +604,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeAr
             cur_row = row;
             start_row(row);
         }
-        const int code = unit_code(a, u, u_end);
+        const int code = unit_code(a, row, int(u - int64_t(row) * a.slots_per_row));
         if (code < 0) continue;
         const int valid = code & 63, phys = code >> 6;
         const int g = row % a.num_kv_heads;
