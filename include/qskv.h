@@ -97,9 +97,10 @@ typedef struct {
  * Bytes of workspace one decode step needs on the current device (the three
  * calls may share one buffer).  The workspace must be 256-byte aligned and
  * zero-filled once before first use (e.g. cudaMemsetAsync); every call
- * leaves it ready for the next one.  It holds the device error word, per-row
- * completion counters, a score buffer for callers that pass none, and the
- * split partial outputs (one slot per row plus one per decode warp).  Calls
+ * leaves it ready for the next one.  It holds the device error word, the
+ * per-row completion counters of page selection, a score buffer for callers
+ * that pass none, and the split partial outputs of decode (one slot per row
+ * plus one per decode warp).  Calls
  * sharing a workspace must not run concurrently on different streams.
  * Returns 0 if the shape is invalid or the device cannot be queried.
  */
@@ -168,13 +169,13 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
  * the device) is not allowed.  The pages have no counterpart of this call.
  *
  * Same arguments and results as qskv_sparse_paged_decode minus the
- * workspace.  The split partials, row counters and error word live in an
- * 8 MiB array of device memory built into the library (every GPU that loads
- * the library holds it until the process exits).  A shape whose scratch
- * (256 B + 4 B per row + (rows + 8 x SM count) x G x (head_dim + 1) x 4 B)
- * exceeds 8 MiB is rejected with QSKV_ERR_WORKSPACE before any launch.
- * Each call clears the error word and the counters with cudaMemsetAsync on
- * `stream`; nothing is allocated or freed.  Device-side index errors still
+ * workspace.  The split partials and the error word live in an 8 MiB array
+ * of device memory built into the library (every GPU that loads the library
+ * holds it until the process exits).  A shape whose scratch (about 256 B +
+ * (rows + 8 x SM count) x G x (head_dim + 1) x 4 B, rows = batch x
+ * num_kv_heads) exceeds 8 MiB is rejected with QSKV_ERR_WORKSPACE before any
+ * launch.  Each call clears the error word with cudaMemsetAsync on `stream`;
+ * nothing is allocated or freed.  Device-side index errors still
  * skip the offending page but are not reported (no workspace to read them
  * from): use qskv_sparse_paged_decode to diagnose.
  * The first call on a device looks up the array's device address with that

@@ -16,9 +16,10 @@
 // whatever the row lengths.  A warp keeps an online softmax per query head of
 // the group; at the end of each row it owns a piece of, it either writes the
 // final output (it owns the whole row) or a normalised partial output with
-// its log-sum-exp into slot (row + warp) of the workspace and takes a ticket
-// on the row; the warp that completes the row merges the partials.  No warp
-// ever waits for another.
+// its log-sum-exp into slot (row + warp) of the workspace.  A second, small
+// kernel merges the partials of the split rows.  Both are launched with
+// programmatic dependent launch, so the merge kernel is resident and waiting
+// when the decode grid drains.  No warp ever waits for another.
 //
 // bf16 KV (tensor cores).  Each warp runs its own pipeline of `stages`
 // shared-memory buffers filled by 2-D TMA tiled loads (16 tokens x 64 dims
@@ -102,129 +103,68 @@ __device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t 
     w1 = last / a.units_per_warp;
 }
 
-// One warp merges the partials of row `row` from warps w0..w1 (slots row+w):
-// out = sum_s 2^(lse_s - max) o_s / sum_s 2^(lse_s - max), in one pass with
-// a running maximum.  Each lane owns up to four float4 positions of the
-// row's G x D output and loads four slots' partials for all of them at once,
-// so a merge costs a few L2 round trips whatever the number of slots.
+// LSE merge of the split partials (one CTA per row).  Row `row` was split
+// over warps w0..w1; warp w left a normalised partial o_w and its log2-domain
+// log-sum-exp in slot row + w.  out = sum_w 2^(lse_w - m) o_w /
+// sum_w 2^(lse_w - m), lse = m + log2 sum_w 2^(lse_w - m), taken in one pass
+// with a running maximum m; each thread owns one float4 of the row's G x D
+// output and keeps eight slots' loads in flight.  Rows a single warp covered
+// were finished by that warp.
 template <int D>
-__device__ void merge_row(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
+__global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int row = blockIdx.x;
+    int64_t w0, w1;
+    row_warps(a, row, w0, w1);
+    if (w0 == w1) return;
     constexpr int V4 = D / 4;
-    constexpr int IT = 4;  // float4 positions per lane per pass
-    constexpr int SC = 4;  // slots per batch of loads
-    const int lane = threadIdx.x & 31;
+    constexpr int SC = 8;
     const int G = a.group;
     const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
     const int ns = int(w1 - w0 + 1);
-    const int n_items = G * V4;
     const float *lse_base = a.part_lse + (row + w0) * G;
     const float4 *o_base = reinterpret_cast<const float4 *>(a.part_o) + (row + w0) * G * V4;
     const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
-    for (int i0 = 0; i0 < n_items; i0 += 32 * IT) {
-        float mx[IT], den[IT];
-        float4 acc[IT];
-#pragma unroll
-        for (int k = 0; k < IT; k++) {
-            mx[k] = -INFINITY;
-            den[k] = 0.f;
-            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+    for (int it = threadIdx.x; it < G * V4; it += blockDim.x) {
+        const int h = it / V4, c4 = it % V4;
+        float mx = -INFINITY, den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s0 = 0; s0 < ns; s0 += SC) {
-            float l[SC][IT];
-            float4 v[SC][IT];
+            float l[SC];
+            float4 v[SC];
 #pragma unroll
             for (int j = 0; j < SC; j++) {
-#pragma unroll
-                for (int k = 0; k < IT; k++) {
-                    const int it = i0 + lane + 32 * k;
-                    const bool ok = it < n_items && s0 + j < ns;
-                    l[j][k] = ok ? __ldcg(lse_base + (s0 + j) * G + it / V4) : -INFINITY;
-                    v[j][k] = ok ? __ldcg(o_base + (s0 + j) * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                const bool ok = s0 + j < ns;
+                l[j] = ok ? __ldcg(lse_base + (s0 + j) * G + h) : -INFINITY;
+                v[j] = ok ? __ldcg(o_base + (s0 + j) * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            float m = mx;
 #pragma unroll
-            for (int k = 0; k < IT; k++) {
-                float m = mx[k];
+            for (int j = 0; j < SC; j++) m = fmaxf(m, l[j]);
+            if (m == -INFINITY) continue;
+            const float sc = exp2f(mx - m);
+            den *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
 #pragma unroll
-                for (int j = 0; j < SC; j++) m = fmaxf(m, l[j][k]);
-                if (m == -INFINITY) continue;
-                const float sc = exp2f(mx[k] - m);
-                den[k] *= sc;
-                acc[k].x *= sc;
-                acc[k].y *= sc;
-                acc[k].z *= sc;
-                acc[k].w *= sc;
-#pragma unroll
-                for (int j = 0; j < SC; j++) {
-                    const float w = exp2f(l[j][k] - m);
-                    den[k] += w;
-                    acc[k].x = fmaf(w, v[j][k].x, acc[k].x);
-                    acc[k].y = fmaf(w, v[j][k].y, acc[k].y);
-                    acc[k].z = fmaf(w, v[j][k].z, acc[k].z);
-                    acc[k].w = fmaf(w, v[j][k].w, acc[k].w);
-                }
-                mx[k] = m;
+            for (int j = 0; j < SC; j++) {
+                const float w = exp2f(l[j] - m);
+                den += w;
+                acc.x = fmaf(w, v[j].x, acc.x);
+                acc.y = fmaf(w, v[j].y, acc.y);
+                acc.z = fmaf(w, v[j].z, acc.z);
+                acc.w = fmaf(w, v[j].w, acc.w);
             }
+            mx = m;
         }
-#pragma unroll
-        for (int k = 0; k < IT; k++) {
-            const int it = i0 + lane + 32 * k;
-            if (it >= n_items) continue;
-            const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;
-            const int h = it / V4, c4 = it % V4;
-            reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
-                make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
-            if (c4 == 0 && a.lse) a.lse[qh0 + h] = den[k] > 0.f ? (mx[k] + log2f(den[k])) * kLn2 : -INFINITY;
-        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (c4 == 0 && a.lse) a.lse[qh0 + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
     }
-}
-
-// After this warp wrote its partial for `row`: take a ticket; the last
-// contributor merges and re-arms the counter.
-template <int D>
-__device__ __forceinline__ void arrive_row(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
-    const int lane = threadIdx.x & 31;
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(a.tickets + row, 1) == int(w1 - w0);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-        __threadfence();
-        merge_row<D>(a, row, w0, w1);
-        if (lane == 0) a.tickets[row] = 0;
-    }
-}
-
-// Deferred arrivals: lane i of the warp holds the i-th row whose partial this
-// warp wrote and has not yet reported (-1 for none).  Reporting them all at
-// once -- one fence, one ticket per row in parallel lanes, then the merges
-// this warp completes -- keeps those round trips out of the streaming loop.
-template <int D>
-__device__ __forceinline__ void arrive_deferred(const DecodeArgs &a, int &drow, int &dcount) {
-    if (dcount == 0) return;
-    const int lane = threadIdx.x & 31;
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane < dcount) {
-        int64_t w0, w1;
-        row_warps(a, drow, w0, w1);
-        last = atomicAdd(a.tickets + drow, 1) == int(w1 - w0);
-    }
-    unsigned mask = __ballot_sync(0xffffffffu, last);
-    if (mask) __threadfence();
-    while (mask) {
-        const int i = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int r = __shfl_sync(0xffffffffu, drow, i);
-        int64_t w0, w1;
-        row_warps(a, r, w0, w1);
-        merge_row<D>(a, r, w0, w1);
-        if (lane == 0) a.tickets[r] = 0;
-    }
-    drow = -1;
-    dcount = 0;
 }
 
 // ------------------------------------------------- bf16 KV, tensor cores --
@@ -248,6 +188,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
     const int64_t u_begin = gw * a.units_per_warp;
     const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
+    pdl_trigger();
     if (u_begin >= u_end) return;
 
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) +
@@ -260,6 +201,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         prefetch_tensormap(&tmap_v);
     }
     __syncwarp();
+    pdl_wait();
 
     // Units are walked with (row, slot) cursors, never by dividing the
     // 64-bit unit index in the loop.
@@ -351,7 +293,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         }
     };
 
-    int drow = -1, dcount = 0;  // rows whose partial awaits its ticket (lane i: i-th)
     auto finish_row = [&](int row) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -394,11 +335,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
                 dst[h1 * ldh + d0] = o[mt][1] * i1;
                 dst[h1 * ldh + d0 + 8] = o[mt][3] * i1;
             }
-        }
-        if (w0 != w1) {
-            if (dcount == 32) arrive_deferred<D>(a, drow, dcount);
-            if (lane == dcount) drow = row;
-            dcount++;
         }
     };
 
@@ -540,7 +476,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         return;
     }
     if (cur_row >= 0) finish_row(cur_row);
-    arrive_deferred<D>(a, drow, dcount);
 }
 
 // --------------------------------------------------- fp32 KV, CUDA cores --
@@ -552,6 +487,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeAr
     const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
     const int64_t u_begin = gw * a.units_per_warp;
     const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
+    pdl_trigger();
+    pdl_wait();
     if (u_begin >= u_end) return;
     float q[8][PL], o[8][PL], m[8], l[8];
     int cur_row = -1;
@@ -594,7 +531,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeAr
                 }
             }
         }
-        if (w0 != w1) arrive_row<D>(a, row, w0, w1);
     };
 
     for (int64_t u = u_begin; u < u_end; u++) {
@@ -652,8 +588,8 @@ cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtens
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
-    decode_bf16_kernel<D, QF32><<<grid.ctas, kDecodeWarps * 32, smem, stream>>>(*tk, *tv, a);
-    return cudaGetLastError();
+    return launch_pdl(decode_bf16_kernel<D, QF32>, dim3(grid.ctas), dim3(kDecodeWarps * 32), smem, stream, *tk, *tv,
+                      a);
 }
 
 }  // namespace
@@ -690,25 +626,37 @@ size_t decode_smem_bytes(int head_dim, int stages) {
     return stage * size_t(stages) * kDecodeWarps + 1024;
 }
 
+static cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t stream) {
+    const dim3 g(unsigned(int64_t(a.batch) * a.num_kv_heads)), b(128);
+    return head_dim == 128 ? launch_pdl(merge_partials_kernel<128>, g, b, 0, stream, a)
+                           : launch_pdl(merge_partials_kernel<64>, g, b, 0, stream, a);
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
                           int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream) {
     if (a.total_units == 0) return cudaSuccess;
     const bool qf = q_dtype == kDtypeF32;
     if (kv_dtype == kDtypeBf16) {
-        if (head_dim == 128) return qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
-                                       : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
-        return qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
-                  : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+        cudaError_t e;
+        if (head_dim == 128)
+            e = qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
+                   : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
+        else
+            e = qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
+                   : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+        if (e != cudaSuccess) return e;
+        return launch_merge(a, head_dim, stream);
     }
     const dim3 g(grid.ctas), b(kDecodeWarps * 32);
-    if (head_dim == 128) {
-        if (qf) decode_simt_kernel<128, true><<<g, b, 0, stream>>>(a);
-        else decode_simt_kernel<128, false><<<g, b, 0, stream>>>(a);
-    } else {
-        if (qf) decode_simt_kernel<64, true><<<g, b, 0, stream>>>(a);
-        else decode_simt_kernel<64, false><<<g, b, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    cudaError_t e;
+    if (head_dim == 128)
+        e = qf ? launch_pdl(decode_simt_kernel<128, true>, g, b, 0, stream, a)
+               : launch_pdl(decode_simt_kernel<128, false>, g, b, 0, stream, a);
+    else
+        e = qf ? launch_pdl(decode_simt_kernel<64, true>, g, b, 0, stream, a)
+               : launch_pdl(decode_simt_kernel<64, false>, g, b, 0, stream, a);
+    if (e != cudaSuccess) return e;
+    return launch_merge(a, head_dim, stream);
 }
 
 }  // namespace qskv

@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(256) meta_build_kernel(MetaArgs a) {
     constexpr int CPR = ROW_BYTES / 16;
     constexpr int RP = 32 / CPR;  // token rows read in parallel by one warp
     static_assert(CPR >= 1 && CPR <= 32 && 32 % CPR == 0, "row must be 16..512 bytes");
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t tile = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (tile >= int64_t(a.n_list) * a.num_kv_heads) return;
@@ -117,14 +119,11 @@ cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cud
     const int warps = 8;
     const dim3 grid(unsigned((tiles + warps - 1) / warps));
     const dim3 block(32 * warps);
-    if (kv_dtype == kDtypeBf16) {
-        if (head_dim == 128) meta_build_kernel<Bf16Ops, 256><<<grid, block, 0, stream>>>(a);
-        else meta_build_kernel<Bf16Ops, 128><<<grid, block, 0, stream>>>(a);
-    } else {
-        if (head_dim == 128) meta_build_kernel<F32Ops, 512><<<grid, block, 0, stream>>>(a);
-        else meta_build_kernel<F32Ops, 256><<<grid, block, 0, stream>>>(a);
-    }
-    return cudaGetLastError();
+    if (kv_dtype == kDtypeBf16)
+        return head_dim == 128 ? launch_pdl(meta_build_kernel<Bf16Ops, 256>, grid, block, 0, stream, a)
+                               : launch_pdl(meta_build_kernel<Bf16Ops, 128>, grid, block, 0, stream, a);
+    return head_dim == 128 ? launch_pdl(meta_build_kernel<F32Ops, 512>, grid, block, 0, stream, a)
+                           : launch_pdl(meta_build_kernel<F32Ops, 256>, grid, block, 0, stream, a);
 }
 
 }  // namespace qskv

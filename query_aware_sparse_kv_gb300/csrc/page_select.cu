@@ -48,6 +48,8 @@ struct RowInfo {
 };
 
 __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
+    pdl_trigger();
+    pdl_wait();
     RowInfo r;
     r.row = blockIdx.y;
     r.b = r.row / a.num_kv_heads;
@@ -385,18 +387,14 @@ cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype,
     const dim3 block(kSelectThreads);
     const bool qf = q_dtype == kDtypeF32;
     if (meta_dtype == kDtypeBf16) {
-        if (head_dim == 128) {
-            if (qf) score_select_mma_kernel<128, true><<<grid, block, 0, stream>>>(a, score_all);
-            else score_select_mma_kernel<128, false><<<grid, block, 0, stream>>>(a, score_all);
-        } else {
-            if (qf) score_select_mma_kernel<64, true><<<grid, block, 0, stream>>>(a, score_all);
-            else score_select_mma_kernel<64, false><<<grid, block, 0, stream>>>(a, score_all);
-        }
-    } else {
-        if (qf) score_select_simt_kernel<float, true><<<grid, block, 0, stream>>>(a, head_dim, score_all);
-        else score_select_simt_kernel<float, false><<<grid, block, 0, stream>>>(a, head_dim, score_all);
+        if (head_dim == 128)
+            return qf ? launch_pdl(score_select_mma_kernel<128, true>, grid, block, 0, stream, a, score_all)
+                      : launch_pdl(score_select_mma_kernel<128, false>, grid, block, 0, stream, a, score_all);
+        return qf ? launch_pdl(score_select_mma_kernel<64, true>, grid, block, 0, stream, a, score_all)
+                  : launch_pdl(score_select_mma_kernel<64, false>, grid, block, 0, stream, a, score_all);
     }
-    return cudaGetLastError();
+    return qf ? launch_pdl(score_select_simt_kernel<float, true>, grid, block, 0, stream, a, head_dim, score_all)
+              : launch_pdl(score_select_simt_kernel<float, false>, grid, block, 0, stream, a, head_dim, score_all);
 }
 
 }  // namespace qskv

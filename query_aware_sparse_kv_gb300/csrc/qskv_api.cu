@@ -31,8 +31,6 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
     off += 256;
     w.sel_tickets = off;
     off = align256(off + size_t(rows) * 4);
-    w.dec_tickets = off;
-    off = align256(off + size_t(rows) * 4);
     w.scores = off;
     off = align256(off + size_t(rows) * size_t(max_pages) * 4);
     w.slots = rows + decode_grid(num_sms).total_warps;
@@ -294,7 +292,6 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     a.lse = lse;
     a.part_o = reinterpret_cast<float *>(ws + L.part_o);
     a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    a.tickets = reinterpret_cast<int32_t *>(ws + L.dec_tickets);
     a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
     a.batch = shape->batch;
     a.num_q_heads = shape->num_q_heads;
@@ -346,10 +343,9 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     const int G = shape->num_q_heads / shape->num_kv_heads;
     const DecodeGrid grid = decode_grid(sms);
 
-    // Layout inside the static scratch: error word, row counters, partials.
+    // Layout inside the static scratch: error word, then the partials.
     const int64_t slots = rows + grid.total_warps;
-    const size_t off_tickets = 256;
-    const size_t off_part_o = align256(off_tickets + size_t(rows) * 4);
+    const size_t off_part_o = 256;
     const size_t off_part_lse = align256(off_part_o + size_t(slots) * G * shape->head_dim * 4);
     const size_t need = align256(off_part_lse + size_t(slots) * G * 4);
     if (need > kNoallocScratchBytes)
@@ -362,7 +358,7 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "cudaGetSymbolAddress of the decode scratch: %s", cudaGetErrorString(e));
     uint8_t *ws = static_cast<uint8_t *>(scratch);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the error word and the row counters must start at zero on every call
+    // the error word must start at zero on every call
     e = cudaMemsetAsync(ws, 0, off_part_o, st);
     if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "clearing the decode scratch: %s", cudaGetErrorString(e));
 
@@ -378,7 +374,6 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     a.lse = lse;
     a.part_o = reinterpret_cast<float *>(ws + off_part_o);
     a.part_lse = reinterpret_cast<float *>(ws + off_part_lse);
-    a.tickets = reinterpret_cast<int32_t *>(ws + off_tickets);
     a.flags = reinterpret_cast<uint32_t *>(ws);
     a.batch = shape->batch;
     a.num_q_heads = shape->num_q_heads;

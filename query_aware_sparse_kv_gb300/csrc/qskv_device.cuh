@@ -78,6 +78,33 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Every kernel is launched with programmatic stream serialization, so it may
+// start while the previous kernel in the stream drains.  pdl_wait() blocks
+// until that kernel has completed and its writes are visible; no kernel
+// touches global memory before it.  pdl_trigger() lets the next kernel in
+// the stream begin its own launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+#ifdef __CUDACC__
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
+
 // ------------------------------------------------------------------- TMA --
 // 2-D tiled bulk tensor load into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, uint64_t *bar) {
@@ -176,7 +203,6 @@ struct DecodeArgs {
     float *lse;             // [B][Hq] or nullptr
     float *part_o;          // [slots][G][D]
     float *part_lse;        // [slots][G], log2 domain
-    int32_t *tickets;       // [rows], zero between calls
     uint32_t *flags;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages, top_k;
     int32_t slots_per_row;  // top_k (sparse) or max_pages (dense)
