@@ -94,12 +94,21 @@ __global__ void __launch_bounds__(256) meta_build_kernel(MetaArgs a) {
     const int r0 = lane / CPR;
     const uint8_t *base =
         static_cast<const uint8_t *>(a.k_pool) + ((int64_t(p) * a.num_kv_heads + g) * a.page_size) * ROW_BYTES;
+    // every row load of the lane is issued before any is used (P <= 32)
+    constexpr int ITER = 32 / RP;
+    uint4 v[ITER];
+#pragma unroll
+    for (int i = 0; i < ITER; i++) {
+        const int r = r0 + i * RP;
+        v[i] = r < valid ? ldg_stream_v4(base + int64_t(r) * ROW_BYTES + c * 16) : Ops::highest();
+    }
     uint4 mn = Ops::highest(), mx = Ops::lowest();
-#pragma unroll 4
-    for (int r = r0; r < valid; r += RP) {
-        const uint4 v = ldg_stream_v4(base + int64_t(r) * ROW_BYTES + c * 16);
-        mn = vmin4<Ops>(mn, v);
-        mx = vmax4<Ops>(mx, v);
+#pragma unroll
+    for (int i = 0; i < ITER; i++) {
+        if (r0 + i * RP < valid) {
+            mn = vmin4<Ops>(mn, v[i]);
+            mx = vmax4<Ops>(mx, v[i]);
+        }
     }
 #pragma unroll
     for (int off = CPR; off < 32; off <<= 1) {

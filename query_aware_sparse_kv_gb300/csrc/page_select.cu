@@ -20,13 +20,13 @@
 // in fp32; fp32 queries are split as hi + lo bf16 pairs (two mma per step).
 // The same identity runs on CUDA cores (fp32 FMA) for fp32 metadata.
 //
-// Selection.  Each CTA scores up to 256 pages of one row and takes a ticket
-// on the row's counter; the CTA that arrives last (no waiting: the others
-// have already left) ranks the whole row.  Scores map to order-preserving
-// 32-bit keys; an MSB-first radix select over 8-bit digits, starting at the
-// highest bit where the row's keys differ, finds the K-th key; a stable
-// compaction in page order keeps every key above it and the lowest-index
-// keys equal to it.  The selected list comes out in ascending page order.
+// Selection.  A second kernel (launched with programmatic dependent launch,
+// so it is resident when scoring drains) ranks each row in one CTA.  Scores
+// map to order-preserving 32-bit keys; an MSB-first radix select over 8-bit
+// digits, starting at the highest bit where the row's keys differ, finds the
+// K-th key; a stable compaction in page order keeps every key above it and
+// the lowest-index keys equal to it.  The selected list comes out in
+// ascending page order.
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
 
@@ -114,11 +114,31 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
     auto key_at = [&](int i) -> uint32_t { return in_smem ? s_keys[i] : order_key(__ldcg(srow + i)); };
 
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int i = tid; i < n_b; i += NT) {
-        const uint32_t k = order_key(__ldcg(srow + i));
-        if (in_smem) s_keys[i] = k;
-        kmin = min(kmin, k);
-        kmax = max(kmax, k);
+    if (in_smem) {
+        // all of this thread's scores are requested before any is used
+        constexpr int PER = kSelectKeyCap / NT;
+        float v[PER];
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            const int i = tid + j * NT;
+            v[j] = i < n_b ? __ldcg(srow + i) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            const int i = tid + j * NT;
+            if (i < n_b) {
+                const uint32_t k = order_key(v[j]);
+                s_keys[i] = k;
+                kmin = min(kmin, k);
+                kmax = max(kmax, k);
+            }
+        }
+    } else {
+        for (int i = tid; i < n_b; i += NT) {
+            const uint32_t k = order_key(__ldcg(srow + i));
+            kmin = min(kmin, k);
+            kmax = max(kmax, k);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -214,132 +234,145 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
     if (tid == 0) a.n_selected[row] = K;
 }
 
-// Ticket on the row counter; the last CTA of the row ranks it.
-__device__ __forceinline__ void finish_row(const SelectArgs &a, const RowInfo &r, const float *srow) {
-    __shared__ int s_last;
-    __threadfence();  // this thread's score writes are visible before the ticket
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int t = atomicAdd(&a.tickets[r.row], 1);
-        s_last = (t == int(gridDim.x) - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) a.tickets[r.row] = 0;
-    select_row(a, r.row, r.n_b, srow);
+// One CTA per row: rank the row's scores.
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int row = blockIdx.x;
+    const int b = row / a.num_kv_heads;
+    int seq = a.seq_lens[b];
+    const int cap = a.max_pages * a.page_size;
+    seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
+    const int n_b = (seq + a.page_size - 1) / a.page_size;
+    select_row(a, row, n_b, a.scores + int64_t(row) * a.max_pages);
 }
 
 // ---------------------------------------------- scores on tensor cores --
 template <int D, bool QF32>
-__global__ void __launch_bounds__(kSelectThreads) score_select_mma_kernel(SelectArgs a, int score_all) {
+__global__ void __launch_bounds__(kScoreThreads) score_mma_kernel(SelectArgs a, int score_all) {
     constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
     const RowInfo r = row_info(a);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gid = lane >> 2;
     float *srow = a.scores + int64_t(r.row) * a.max_pages;
-    const int cta_page0 = blockIdx.x * kSelectThreads;
+    const int w_page0 = blockIdx.x * kScoreThreads + warp * 32;  // this warp's 32 pages: 2 groups of 16
+    if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
 
-    if (cta_page0 < r.n_b && (a.top_k < r.n_b || score_all)) {
-        // B operand: the [q- | q+] column of head gid of the group, in the
-        // chunk order this lane uses for the metadata rows.
-        uint32_t bh[NKP][4], bl[NKP][4];
-        const bool head_ok = gid < a.group;
-        const int64_t qoff = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * a.group + (head_ok ? gid : 0)) * D;
+    // Every load of the warp is issued before any is used: q, the page ids,
+    // then the metadata rows of both groups.
+    const bool head_ok = gid < a.group;
+    const int64_t qoff = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * a.group + (head_ok ? gid : 0)) * D;
+    uint4 qraw[NKP][QF32 ? 2 : 1];
 #pragma unroll
-        for (int kp = 0; kp < NKP; kp++) {
-            const int c = 4 * kp + t;
-            const bool upper = 8 * c >= D;  // chunk of the M half: pairs with q+
-            const int col = 8 * c - (upper ? D : 0);
-            float v[8];
-            if (QF32) {
-                const float4 *qp = reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + qoff + col);
-                const float4 x0 = qp[0], x1 = qp[1];
-                v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-            } else {
-                const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff + col);
-                v[0] = bf16_lo_to_float(x.x); v[1] = bf16_hi_to_float(x.x);
-                v[2] = bf16_lo_to_float(x.y); v[3] = bf16_hi_to_float(x.y);
-                v[4] = bf16_lo_to_float(x.z); v[5] = bf16_hi_to_float(x.z);
-                v[6] = bf16_lo_to_float(x.w); v[7] = bf16_hi_to_float(x.w);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                v[i] = upper ? fmaxf(v[i], 0.f) : fminf(v[i], 0.f);
-                if (!head_ok) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                bh[kp][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                if (QF32) {
-                    const float r0 = v[2 * i] - bf16_lo_to_float(bh[kp][i]);
-                    const float r1 = v[2 * i + 1] - bf16_hi_to_float(bh[kp][i]);
-                    bl[kp][i] = pack_bf16x2(r0, r1);
-                }
-            }
+    for (int kp = 0; kp < NKP; kp++) {
+        const int c = 4 * kp + t;
+        const int col = 8 * c - (8 * c >= D ? D : 0);
+        if (QF32) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + qoff + col);
+            qraw[kp][0] = qp[0];
+            qraw[kp][QF32 ? 1 : 0] = qp[1];
+        } else {
+            qraw[kp][0] = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff + col);
         }
+    }
+    const int32_t *trow = a.page_table + int64_t(r.b) * a.max_pages;
+    int jj[4], pp[4];
+    bool vv[4], bad[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {  // rows gid, gid+8 of group 0, then of group 1
+        jj[i] = w_page0 + (i >> 1) * 16 + gid + (i & 1) * 8;
+        vv[i] = jj[i] < r.n_b;
+        pp[i] = vv[i] ? trow[jj[i]] : 0;
+    }
+    const char *meta = static_cast<const char *>(a.meta);
+    uint4 av[4][NKP];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        bad[i] = vv[i] && (pp[i] < 0 || pp[i] >= a.num_pool_pages);
+        const char *rowp = meta + (int64_t(bad[i] ? 0 : pp[i]) * a.num_kv_heads + r.g) * (2 * D * 2);
+#pragma unroll
+        for (int kp = 0; kp < NKP; kp++)
+            av[i][kp] = (vv[i] && !bad[i]) ? ldg_stream_v4(rowp + (4 * kp + t) * 16) : make_uint4(0, 0, 0, 0);
+    }
+    if ((bad[0] || bad[1] || bad[2] || bad[3]) && t == 0) raise_error(a.flags, kErrPageId);
 
-        const char *meta = static_cast<const char *>(a.meta);
-        const int32_t *trow = a.page_table + int64_t(r.b) * a.max_pages;
-#pragma unroll 1
-        for (int grp = 0; grp < 2; grp++) {
-            const int j0 = cta_page0 + warp * 32 + grp * 16;
-            if (j0 >= r.n_b) break;
-            const int ja = j0 + gid, jb = j0 + gid + 8;
-            const bool va = ja < r.n_b, vb = jb < r.n_b;
-            int pa = va ? trow[ja] : 0, pb = vb ? trow[jb] : 0;
-            const bool bada = va && (pa < 0 || pa >= a.num_pool_pages);
-            const bool badb = vb && (pb < 0 || pb >= a.num_pool_pages);
-            if ((bada || badb) && t == 0) raise_error(a.flags, kErrPageId);
-            uint4 av[NKP], bv[NKP];
-            const char *rowa = meta + (int64_t(pa) * a.num_kv_heads + r.g) * (2 * D * 2);
-            const char *rowb = meta + (int64_t(pb) * a.num_kv_heads + r.g) * (2 * D * 2);
+    // B operand: the [q- | q+] column of head gid of the group, in the chunk
+    // order this lane uses for the metadata rows.
+    uint32_t bh[NKP][4], bl[NKP][4];
 #pragma unroll
-            for (int kp = 0; kp < NKP; kp++) {
-                const int c = 4 * kp + t;
-                av[kp] = (va && !bada) ? ldg_stream_v4(rowa + c * 16) : make_uint4(0, 0, 0, 0);
-                bv[kp] = (vb && !badb) ? ldg_stream_v4(rowb + c * 16) : make_uint4(0, 0, 0, 0);
-            }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kp = 0; kp < NKP; kp++) {
+        const bool upper = 8 * (4 * kp + t) >= D;  // chunk of the M half: pairs with q+
+        float v[8];
+        if (QF32) {
+            const uint4 x0 = qraw[kp][0], x1 = qraw[kp][QF32 ? 1 : 0];
+            v[0] = __uint_as_float(x0.x); v[1] = __uint_as_float(x0.y);
+            v[2] = __uint_as_float(x0.z); v[3] = __uint_as_float(x0.w);
+            v[4] = __uint_as_float(x1.x); v[5] = __uint_as_float(x1.y);
+            v[6] = __uint_as_float(x1.z); v[7] = __uint_as_float(x1.w);
+        } else {
+            const uint4 x = qraw[kp][0];
+            v[0] = bf16_lo_to_float(x.x); v[1] = bf16_hi_to_float(x.x);
+            v[2] = bf16_lo_to_float(x.y); v[3] = bf16_hi_to_float(x.y);
+            v[4] = bf16_lo_to_float(x.z); v[5] = bf16_hi_to_float(x.z);
+            v[6] = bf16_lo_to_float(x.w); v[7] = bf16_hi_to_float(x.w);
+        }
 #pragma unroll
-            for (int kp = 0; kp < NKP; kp++) {
-                const uint32_t fa0[4] = {av[kp].x, bv[kp].x, av[kp].y, bv[kp].y};
-                const uint32_t fa1[4] = {av[kp].z, bv[kp].z, av[kp].w, bv[kp].w};
-                mma_bf16_16816(acc, fa0, bh[kp][0], bh[kp][1]);
-                mma_bf16_16816(acc, fa1, bh[kp][2], bh[kp][3]);
-                if (QF32) {
-                    mma_bf16_16816(acc, fa0, bl[kp][0], bl[kp][1]);
-                    mma_bf16_16816(acc, fa1, bl[kp][2], bl[kp][3]);
-                }
-            }
-            // acc: [page gid][head 2t], [gid][2t+1], [gid+8][2t], [gid+8][2t+1]
-            const float NEG = -INFINITY;
-            const bool h0 = 2 * t < a.group, h1 = 2 * t + 1 < a.group;
-            float sa = fmaxf(h0 ? acc[0] : NEG, h1 ? acc[1] : NEG);
-            float sb = fmaxf(h0 ? acc[2] : NEG, h1 ? acc[3] : NEG);
-            sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 1));
-            sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 2));
-            sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 1));
-            sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 2));
-            if (t == 0) {
-                if (va) srow[ja] = bada ? NEG : sa;
-                if (vb) srow[jb] = badb ? NEG : sb;
+        for (int i = 0; i < 8; i++) {
+            v[i] = upper ? fmaxf(v[i], 0.f) : fminf(v[i], 0.f);
+            if (!head_ok) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            bh[kp][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            if (QF32) {
+                const float r0 = v[2 * i] - bf16_lo_to_float(bh[kp][i]);
+                const float r1 = v[2 * i + 1] - bf16_hi_to_float(bh[kp][i]);
+                bl[kp][i] = pack_bf16x2(r0, r1);
             }
         }
     }
-    finish_row(a, r, srow);
+
+    const float NEG = -INFINITY;
+    const bool h0 = 2 * t < a.group, h1 = 2 * t + 1 < a.group;
+#pragma unroll
+    for (int grp = 0; grp < 2; grp++) {
+        const int ia = 2 * grp, ib = 2 * grp + 1;
+        if (w_page0 + grp * 16 >= r.n_b) break;  // warp-uniform: the group holds no page
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kp = 0; kp < NKP; kp++) {
+            const uint32_t fa0[4] = {av[ia][kp].x, av[ib][kp].x, av[ia][kp].y, av[ib][kp].y};
+            const uint32_t fa1[4] = {av[ia][kp].z, av[ib][kp].z, av[ia][kp].w, av[ib][kp].w};
+            mma_bf16_16816(acc, fa0, bh[kp][0], bh[kp][1]);
+            mma_bf16_16816(acc, fa1, bh[kp][2], bh[kp][3]);
+            if (QF32) {
+                mma_bf16_16816(acc, fa0, bl[kp][0], bl[kp][1]);
+                mma_bf16_16816(acc, fa1, bl[kp][2], bl[kp][3]);
+            }
+        }
+        // acc: [page gid][head 2t], [gid][2t+1], [gid+8][2t], [gid+8][2t+1]
+        float sa = fmaxf(h0 ? acc[0] : NEG, h1 ? acc[1] : NEG);
+        float sb = fmaxf(h0 ? acc[2] : NEG, h1 ? acc[3] : NEG);
+        sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 1));
+        sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 2));
+        sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 1));
+        sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 2));
+        if (t == 0) {
+            if (vv[ia]) srow[jj[ia]] = bad[ia] ? NEG : sa;
+            if (vv[ib]) srow[jj[ib]] = bad[ib] ? NEG : sb;
+        }
+    }
 }
 
 // -------------------------------------------------- scores on CUDA cores --
 template <typename MT, bool QF32>
-__global__ void __launch_bounds__(kSelectThreads) score_select_simt_kernel(SelectArgs a, int D, int score_all) {
+__global__ void __launch_bounds__(kScoreThreads) score_simt_kernel(SelectArgs a, int D, int score_all) {
     __shared__ float s_qp[8][128];
     __shared__ float s_qn[8][128];
     const RowInfo r = row_info(a);
     float *srow = a.scores + int64_t(r.row) * a.max_pages;
-    const int j = blockIdx.x * kSelectThreads + threadIdx.x;
-    const bool work = int(blockIdx.x) * kSelectThreads < r.n_b && (a.top_k < r.n_b || score_all);
+    const int j = blockIdx.x * kScoreThreads + threadIdx.x;
+    const bool work = int(blockIdx.x) * kScoreThreads < r.n_b && (a.top_k < r.n_b || score_all);
     if (work) {
         for (int e = threadIdx.x; e < a.group * D; e += blockDim.x) {
             const int h = e / D, c = e % D;
@@ -375,7 +408,6 @@ __global__ void __launch_bounds__(kSelectThreads) score_select_simt_kernel(Selec
             srow[j] = best;
         }
     }
-    finish_row(a, r, srow);
 }
 
 }  // namespace
@@ -383,18 +415,23 @@ __global__ void __launch_bounds__(kSelectThreads) score_select_simt_kernel(Selec
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
                                int score_all) {
     const int64_t rows = int64_t(a.batch) * a.num_kv_heads;
-    const dim3 grid(unsigned((a.max_pages + kSelectThreads - 1) / kSelectThreads), unsigned(rows));
-    const dim3 block(kSelectThreads);
+    const dim3 grid(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
+    const dim3 block(kScoreThreads);
     const bool qf = q_dtype == kDtypeF32;
+    cudaError_t e;
     if (meta_dtype == kDtypeBf16) {
         if (head_dim == 128)
-            return qf ? launch_pdl(score_select_mma_kernel<128, true>, grid, block, 0, stream, a, score_all)
-                      : launch_pdl(score_select_mma_kernel<128, false>, grid, block, 0, stream, a, score_all);
-        return qf ? launch_pdl(score_select_mma_kernel<64, true>, grid, block, 0, stream, a, score_all)
-                  : launch_pdl(score_select_mma_kernel<64, false>, grid, block, 0, stream, a, score_all);
+            e = qf ? launch_pdl(score_mma_kernel<128, true>, grid, block, 0, stream, a, score_all)
+                   : launch_pdl(score_mma_kernel<128, false>, grid, block, 0, stream, a, score_all);
+        else
+            e = qf ? launch_pdl(score_mma_kernel<64, true>, grid, block, 0, stream, a, score_all)
+                   : launch_pdl(score_mma_kernel<64, false>, grid, block, 0, stream, a, score_all);
+    } else {
+        e = qf ? launch_pdl(score_simt_kernel<float, true>, grid, block, 0, stream, a, head_dim, score_all)
+               : launch_pdl(score_simt_kernel<float, false>, grid, block, 0, stream, a, head_dim, score_all);
     }
-    return qf ? launch_pdl(score_select_simt_kernel<float, true>, grid, block, 0, stream, a, head_dim, score_all)
-              : launch_pdl(score_select_simt_kernel<float, false>, grid, block, 0, stream, a, head_dim, score_all);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_kernel, dim3(unsigned(rows)), dim3(kSelectThreads), 0, stream, a);
 }
 
 }  // namespace qskv

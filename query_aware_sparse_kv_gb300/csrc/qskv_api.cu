@@ -29,8 +29,6 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
     size_t off = 0;
     w.flags = off;
     off += 256;
-    w.sel_tickets = off;
-    off = align256(off + size_t(rows) * 4);
     w.scores = off;
     off = align256(off + size_t(rows) * size_t(max_pages) * 4);
     w.slots = rows + decode_grid(num_sms).total_warps;
@@ -238,7 +236,6 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     a.selected = selected;
     a.n_selected = n_selected;
     a.scores = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
-    a.tickets = reinterpret_cast<int32_t *>(ws + L.sel_tickets);
     a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
     a.batch = shape->batch;
     a.num_q_heads = shape->num_q_heads;

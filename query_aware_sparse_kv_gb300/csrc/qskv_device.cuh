@@ -186,7 +186,6 @@ struct SelectArgs {
     int32_t *selected;      // [rows][top_k]
     int32_t *n_selected;    // [rows]
     float *scores;          // [rows][max_pages]
-    int32_t *tickets;       // [rows], zero between calls
     uint32_t *flags;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages, top_k;
 };
@@ -212,7 +211,8 @@ struct DecodeArgs {
     float scale_log2;       // sm_scale * log2(e)
 };
 
-constexpr int kSelectThreads = 256;   // pages scored per CTA = kSelectThreads
+constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
+constexpr int kSelectThreads = 256;   // ranking CTA: one row
 constexpr int kSelectKeyCap = 4096;   // keys held in shared memory by the select stage
 constexpr int kDecodeWarps = 4;       // warps per decode CTA
 constexpr int kDecodeCtasPerSm = 2;   // decode grid = this x SM count

@@ -18,7 +18,6 @@ struct DecodeArgs;
 // Workspace layout: every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
     size_t flags;        // uint32 error word (+ padding to 256 B)
-    size_t sel_tickets;  // int32 [rows]
     size_t scores;       // fp32  [rows][max_pages]
     size_t part_o;       // fp32  [slots][G][D]
     size_t part_lse;     // fp32  [slots][G]
