@@ -39,6 +39,7 @@
 //
 // fp32 KV runs a CUDA-core kernel with the same decomposition and merge.
 #include <mutex>
+#include <type_traits>
 
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
             for (int j = 0; j < SC; j++) {
                 const bool ok = s0 + j < ns;
                 l[j] = ok ? __ldcg(lse_base + (s0 + j) * G + h) : -INFINITY;
-                v[j] = ok ? __ldcg(o_base + (s0 + j) * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[j] = ok && l[j] != -INFINITY ? __ldcg(o_base + (s0 + j) * G * V4 + it)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float m = mx;
 #pragma unroll
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
             acc.w *= sc;
 #pragma unroll
             for (int j = 0; j < SC; j++) {
+                if (l[j] == -INFINITY) continue;  // an empty piece: its o was never written
                 const float w = exp2f(l[j] - m);
                 den += w;
                 acc.x = fmaf(w, v[j].x, acc.x);
@@ -168,24 +171,48 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------- bf16 KV, tensor cores --
-template <int D, bool QF32>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
+// Pieces of rows a warp's range touches but that hold no sub-tile for it:
+// an empty contribution (lse = -inf), or the final empty answer when the
+// warp owns the row alone.
+template <int D>
+__device__ void write_empty_piece(const DecodeArgs &a, int row, int64_t gw) {
+    const int lane = threadIdx.x & 31;
+    const int G = a.group;
+    int64_t w0, w1;
+    row_warps(a, row, w0, w1);
+    if (w0 == w1) {
+        const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+        const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+        for (int i = lane; i < G * D; i += 32) a.out[qh0 * D + i] = 0.f;
+        if (a.lse && lane < G) a.lse[qh0 + lane] = -INFINITY;
+    } else if (lane < G) {
+        a.part_lse[(row + gw) * G + lane] = -INFINITY;
+    }
+}
+
+// A stage holds up to HALVES 16-token sub-tiles ("halves") of one row: K
+// then V, each half as D/64 boxes of 16 tokens x 64 dims (128-byte swizzle).
+template <int D, bool QF32, int WPC, int HALVES>
+__global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        DecodeArgs a) {
-    constexpr int NB = D / 64;          // 64-dim boxes per token row
-    constexpr int BOX = 16 * 128;       // bytes of one box: 16 tokens x 128 B
-    constexpr int KVB = NB * BOX;       // K (or V) bytes of a 16-token sub-tile
+    static_assert(HALVES == 1 || HALVES == 2, "a stage holds one or two 16-token halves");
+    constexpr int NB = D / 64;            // 64-dim boxes per token row
+    constexpr int BOX = 16 * 128;         // bytes of one box: 16 tokens x 128 B
+    constexpr int HALF = NB * BOX;        // K (or V) bytes of one 16-token sub-tile
+    constexpr int KVB = HALVES * HALF;    // K (or V) bytes of a stage
     constexpr int STAGE = 2 * KVB;
-    constexpr int NKS = D / 16;         // k-steps of Q.K^T, m-tiles of P.V
+    constexpr int NKS = D / 16;           // k-steps of Q.K^T, m-tiles of P.V
+    constexpr float kLazy = 8.f;          // rescale only when a head's max grows by > 2^8
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kDecodeWarps][kMaxStages];
+    __shared__ __align__(8) uint64_t bars[WPC][kMaxStages];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gid = lane >> 2;
     const int S = a.stages;
     const int G = a.group;
-    const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
+    const int64_t gw = int64_t(blockIdx.x) * WPC + warp;
     const int64_t u_begin = gw * a.units_per_warp;
     const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
     pdl_trigger();
@@ -208,9 +235,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     const int spr = a.slots_per_row;
     const int row_begin = int(u_begin / spr);
     const int slot_begin = int(u_begin - int64_t(row_begin) * spr);
+    const int row_last = int((u_end - 1) / spr);
 
     // Codes of units [wbase, wbase + 64): lane i holds units wbase+i and
-    // wbase+32+i; (wrow, wslot) are the coordinates of wbase.
+    // wbase+32+i; (wrow, wslot) are the coordinates of wbase.  Only the
+    // producer reads them; it slides the window.
     int64_t wbase = u_begin;
     int wrow = row_begin, wslot = slot_begin;
     int code_cur = unit_code_at(a, wrow, wslot, lane, wbase, u_end);
@@ -222,40 +251,82 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         return k < 32 ? c0 : c1;
     };
 
-    // ---------------- producer: lane 0 issues TMA for the next sub-tiles
+    // ---------------- producer: fills a stage with the next one or two
+    // sub-tiles of one row; lane s remembers stage s's row and valid counts.
     int64_t pu = u_begin;
-    int pslot = slot_begin, pg = row_begin % a.num_kv_heads;
+    int prow = row_begin, pslot = slot_begin, pg = row_begin % a.num_kv_heads;
     int psub = 0, ps = 0;
     uint32_t issued = 0, consumed = 0;
+    int st_row = 0, st_valid = 0;  // lane s: stage s's row; valid tokens half0 | half1 << 8
+    auto advance_sub = [&](int nsub) {
+        if (++psub >= nsub) {
+            psub = 0;
+            pu++;
+            if (++pslot == spr) {
+                pslot = 0;
+                prow++;
+                if (++pg == a.num_kv_heads) pg = 0;
+            }
+        }
+    };
     auto produce = [&]() {
-        while (int(issued - consumed) < S && pu < u_end && pu - wbase < 64) {
-            const int code = code_of(pu);
-            int nsub = 0;
-            if (code >= 0) {
+        while (int(issued - consumed) < S) {
+            int nh = 0, srow = -1, v0 = 0, v1 = 0, y0 = 0, y1 = 0;
+            while (nh < HALVES && pu < u_end) {
+                if (pu - wbase >= 32) {  // slide the code window by 32 units
+                    wbase += 32;
+                    wslot += 32;
+                    while (wslot >= spr) {
+                        wslot -= spr;
+                        wrow++;
+                    }
+                    code_cur = code_nxt;
+                    code_nxt = unit_code_at(a, wrow, wslot, 32 + lane, wbase, u_end);
+                }
+                const int code = code_of(pu);
+                if (code < 0) {
+                    advance_sub(0);
+                    continue;
+                }
+                if (nh > 0 && prow != srow) break;  // a stage never spans two rows
+                srow = prow;
                 const int valid = code & 63, phys = code >> 6;
-                nsub = (valid + 15) >> 4;
-                if (lane == 0) {
-                    uint8_t *st = ring + size_t(ps) * STAGE;
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar + ps, STAGE);
-                    const int y = (phys * a.num_kv_heads + pg) * a.page_size + psub * 16;
+                const int v = min(16, valid - psub * 16);
+                const int y = (phys * a.num_kv_heads + pg) * a.page_size + psub * 16;
+                if (nh == 0) {
+                    v0 = v;
+                    y0 = y;
+                } else {
+                    v1 = v;
+                    y1 = y;
+                }
+                nh++;
+                advance_sub((valid + 15) >> 4);
+            }
+            if (nh == 0) break;
+            if (lane == 0) {
+                uint8_t *st = ring + size_t(ps) * STAGE;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar + ps, uint32_t(nh) * 2 * HALF);
+#pragma unroll
+                for (int nb = 0; nb < NB; nb++) {
+                    tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y0, bar + ps);
+                    tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y0, bar + ps);
+                }
+                if (HALVES == 2 && nh == 2) {
 #pragma unroll
                     for (int nb = 0; nb < NB; nb++) {
-                        tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y, bar + ps);
-                        tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y, bar + ps);
+                        tma_load_2d(st + HALF + nb * BOX, &tmap_k, nb * 64, y1, bar + ps);
+                        tma_load_2d(st + KVB + HALF + nb * BOX, &tmap_v, nb * 64, y1, bar + ps);
                     }
                 }
-                issued++;
-                ps = ps + 1 == S ? 0 : ps + 1;
             }
-            if (++psub >= nsub) {  // next unit
-                psub = 0;
-                pu++;
-                if (++pslot == spr) {
-                    pslot = 0;
-                    if (++pg == a.num_kv_heads) pg = 0;
-                }
+            if (lane == ps) {
+                st_row = srow;
+                st_valid = v0 | (v1 << 8);
             }
+            issued++;
+            ps = ps + 1 == S ? 0 : ps + 1;
         }
     };
 
@@ -305,12 +376,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         int64_t w0, w1;
         row_warps(a, row, w0, w1);
         float *dst;
-        int64_t ldh;  // floats between heads
         if (w0 == w1) {
             const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
             const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G;
             dst = a.out + qh * D;
-            ldh = D;
             if (a.lse && gid == 0) {
                 if (h0 < G) a.lse[qh + h0] = e0 * kLn2;
                 if (h1 < G) a.lse[qh + h1] = e1 * kLn2;
@@ -318,7 +387,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         } else {
             const int64_t slot = row + gw;
             dst = a.part_o + slot * G * D;
-            ldh = D;
             if (gid == 0) {
                 if (h0 < G) a.part_lse[slot * G + h0] = e0;
                 if (h1 < G) a.part_lse[slot * G + h1] = e1;
@@ -328,125 +396,151 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
         for (int mt = 0; mt < NKS; mt++) {
             const int d0 = mt * 16 + gid;
             if (h0 < G) {
-                dst[h0 * ldh + d0] = o[mt][0] * i0;
-                dst[h0 * ldh + d0 + 8] = o[mt][2] * i0;
+                dst[h0 * D + d0] = o[mt][0] * i0;
+                dst[h0 * D + d0 + 8] = o[mt][2] * i0;
             }
             if (h1 < G) {
-                dst[h1 * ldh + d0] = o[mt][1] * i1;
-                dst[h1 * ldh + d0 + 8] = o[mt][3] * i1;
+                dst[h1 * D + d0] = o[mt][1] * i1;
+                dst[h1 * D + d0 + 8] = o[mt][3] * i1;
             }
         }
     };
 
-    // ---------------- main loop
-    int64_t cu = u_begin;
-    int crow = row_begin, cslot = slot_begin;
-    int csub = 0, cs = 0;
+    // Q.K^T of NH halves (tokens gid / gid+8 x heads 2t / 2t+1), masked;
+    // the halves' accumulation chains are interleaved.
+    auto mask_scale = [&](const float (&sa)[2][4], int valid, float (&s)[4]) {
+        const float sc = a.scale_log2;
+        s[0] = gid < valid ? (sa[0][0] + sa[1][0]) * sc : -INFINITY;
+        s[1] = gid < valid ? (sa[0][1] + sa[1][1]) * sc : -INFINITY;
+        s[2] = gid + 8 < valid ? (sa[0][2] + sa[1][2]) * sc : -INFINITY;
+        s[3] = gid + 8 < valid ? (sa[0][3] + sa[1][3]) * sc : -INFINITY;
+    };
+    auto qk = [&](auto nh_tag, uint32_t kb, int v0, int v1, float (&s0)[4], float (&s1)[4]) {
+        constexpr int NH = decltype(nh_tag)::value;
+        float sa[NH][2][4];
+#pragma unroll
+        for (int h = 0; h < NH; h++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) sa[h][0][i] = sa[h][1][i] = 0.f;
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ks++) {
+            const int c = (ks & 3) * 2 + (mat >> 1);
+            const uint32_t off = (ks >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t af[NH][4];
+#pragma unroll
+            for (int h = 0; h < NH; h++) ldmatrix_x4(af[h], kb + h * HALF + off);
+#pragma unroll
+            for (int h = 0; h < NH; h++) {
+                mma_bf16_16816(sa[h][ks & 1], af[h], qb[ks][0], qb[ks][1]);
+                if (QF32) mma_bf16_16816(sa[h][ks & 1], af[h], ql[ks][0], ql[ks][1]);
+            }
+        }
+        mask_scale(sa[0], v0, s0);
+        if (NH == 2) mask_scale(sa[NH - 1], v1, s1);
+    };
+    // O^T += V^T . P^T for one half.
+    auto pv_half = [&](uint32_t vb, uint32_t pb0, uint32_t pb1) {
+        const int mat = lane >> 3;
+        const int r = (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+        for (int mt = 0; mt < NKS; mt++) {
+            const int c = (mt & 3) * 2 + (mat & 1);
+            uint32_t af[4];
+            ldmatrix_x4_trans(af, vb + (mt >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
+            mma_bf16_16816(o[mt], af, pb0, pb1);
+        }
+    };
+    // Zero the V rows of a half past its valid tokens (they may hold NaN).
+    auto zero_v_tail = [&](uint8_t *vhalf, int valid) {
+        uint4 *vrow = reinterpret_cast<uint4 *>(vhalf);
+        const int n = (16 - valid) * 8;
+        for (int i = lane; i < NB * n; i += 32) {
+            const int nb = i / n, r = valid + (i % n) / 8, c = i % 8;
+            vrow[(nb * BOX + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+        }
+    };
+
+    // ---------------- main loop: one stage (up to 32 tokens of one row) per pass
+    int cs = 0;
     uint32_t cphase = 0;
-    bool aborted = false;
+    int empty_from = row_begin;  // first row not yet given a piece
     produce();
-    while (cu < u_end) {
-        if (cu - wbase >= 32) {  // slide the code window by 32 units
-            wbase += 32;
-            wslot += 32;
-            while (wslot >= spr) {
-                wslot -= spr;
-                wrow++;
-            }
-            code_cur = code_nxt;
-            code_nxt = unit_code_at(a, wrow, wslot, 32 + lane, wbase, u_end);
-        }
-        produce();
-        if (crow != cur_row) {
-            if (cur_row >= 0) finish_row(cur_row);
-            cur_row = crow;
-            start_row(crow);
-        }
-        const int code = code_of(cu);
-        if (code < 0) {
-            cu++;
-            csub = 0;
-            if (++cslot == spr) {
-                cslot = 0;
-                crow++;
-            }
-            continue;
-        }
-        const int valid = code & 63;
-        const int vsub = min(16, valid - csub * 16);
+    while (consumed != issued) {
         if (!mbar_wait_bounded(bar + cs, cphase, kWaitLimitNs)) {
             if (lane == 0) raise_error(a.flags, kErrTimeout);
-            aborted = true;
-            break;
+            // let the copies already issued land before the CTA's memory is released
+            while (consumed != issued) {
+                mbar_wait_bounded(bar + cs, cphase, kWaitLimitNs);
+                consumed++;
+                if (++cs == S) {
+                    cs = 0;
+                    cphase ^= 1u;
+                }
+            }
+            return;
+        }
+        const int row = __shfl_sync(0xffffffffu, st_row, cs);
+        const int vv = __shfl_sync(0xffffffffu, st_valid, cs);
+        const int v0 = vv & 255, v1 = vv >> 8;
+        if (row != cur_row) {
+            if (cur_row >= 0) finish_row(cur_row);
+            for (int r = empty_from; r < row; r++)
+                if (r != cur_row) write_empty_piece<D>(a, r, gw);
+            empty_from = row + 1;
+            cur_row = row;
+            start_row(row);
         }
         uint8_t *st = ring + size_t(cs) * STAGE;
-        if (vsub < 16) {  // zero V rows past the sequence end (they may hold NaN)
-            uint4 *vrow = reinterpret_cast<uint4 *>(st + KVB);
-            const int n = (16 - vsub) * 8;
-            for (int i = lane; i < NB * n; i += 32) {
-                const int nb = i / n, r = vsub + (i % n) / 8, c = i % 8;
-                vrow[(nb * BOX + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
-            }
-            __syncwarp();
-        }
+        if (v0 < 16) zero_v_tail(st + KVB, v0);
+        if (v1 > 0 && v1 < 16) zero_v_tail(st + KVB + HALF, v1);
+        if (v0 < 16 || (v1 > 0 && v1 < 16)) __syncwarp();
         const uint32_t kb = smem_u32(st), vb = kb + KVB;
 
-        // S^T = K . Q^T, as two independent accumulation chains
-        float sacc[4];
-        {
-            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const int mat = lane >> 3;
-            const int r = (lane & 7) + ((mat & 1) << 3);
-#pragma unroll
-            for (int ks = 0; ks < NKS; ks++) {
-                const int c = (ks & 3) * 2 + (mat >> 1);
-                uint32_t af[4];
-                ldmatrix_x4(af, kb + (ks >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
-                mma_bf16_16816(sa[ks & 1], af, qb[ks][0], qb[ks][1]);
-                if (QF32) mma_bf16_16816(sa[ks & 1], af, ql[ks][0], ql[ks][1]);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i++) sacc[i] = sa[0][i] + sa[1][i];
+        float s0[4], s1[4];
+        if (HALVES == 2 && v1 > 0) {
+            qk(std::integral_constant<int, 2>(), kb, v0, v1, s0, s1);
+        } else {
+            qk(std::integral_constant<int, 1>(), kb, v0, v1, s0, s1);
+            s1[0] = s1[1] = s1[2] = s1[3] = -INFINITY;
         }
-        // online softmax; sacc = [tok gid][h0], [gid][h1], [gid+8][h0], [gid+8][h1]
-        const float sc = a.scale_log2;
-        const float s0 = gid < vsub ? sacc[0] * sc : -INFINITY;
-        const float s1 = gid < vsub ? sacc[1] * sc : -INFINITY;
-        const float s2 = gid + 8 < vsub ? sacc[2] * sc : -INFINITY;
-        const float s3 = gid + 8 < vsub ? sacc[3] * sc : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        // s*[0], s*[2]: head 2t; s*[1], s*[3]: head 2t+1
+        float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
+        float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        const uint32_t x0 = pack_bf16x2(exp2f(s0 - n0), exp2f(s1 - n1));
-        const uint32_t x1 = pack_bf16x2(exp2f(s2 - n0), exp2f(s3 - n1));
-        l0 = l0 * al0 + (bf16_lo_to_float(x0) + bf16_lo_to_float(x1));
-        l1 = l1 * al1 + (bf16_hi_to_float(x0) + bf16_hi_to_float(x1));
-#pragma unroll
-        for (int mt = 0; mt < NKS; mt++) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-        }
-        const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
-        // O^T += V^T . P^T
-        {
-            const int mat = lane >> 3;
-            const int r = (lane & 7) + ((mat >> 1) << 3);
+        // lazy rescale: keep the running max unless some head's new max
+        // exceeds it by more than kLazy (then probabilities stay <= 2^kLazy)
+        if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
 #pragma unroll
             for (int mt = 0; mt < NKS; mt++) {
-                const int c = (mt & 3) * 2 + (mat & 1);
-                uint32_t af[4];
-                ldmatrix_x4_trans(af, vb + (mt >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
-                mma_bf16_16816(o[mt], af, pb0, pb1);
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
             }
+        }
+        const uint32_t x00 = pack_bf16x2(exp2f(s0[0] - m0), exp2f(s0[1] - m1));
+        const uint32_t x01 = pack_bf16x2(exp2f(s0[2] - m0), exp2f(s0[3] - m1));
+        l0 += bf16_lo_to_float(x00) + bf16_lo_to_float(x01);
+        l1 += bf16_hi_to_float(x00) + bf16_hi_to_float(x01);
+        pv_half(vb, movmatrix_trans(x00), movmatrix_trans(x01));
+        if (HALVES == 2 && v1 > 0) {
+            const uint32_t x10 = pack_bf16x2(exp2f(s1[0] - m0), exp2f(s1[1] - m1));
+            const uint32_t x11 = pack_bf16x2(exp2f(s1[2] - m0), exp2f(s1[3] - m1));
+            l0 += bf16_lo_to_float(x10) + bf16_lo_to_float(x11);
+            l1 += bf16_hi_to_float(x10) + bf16_hi_to_float(x11);
+            pv_half(vb + HALF, movmatrix_trans(x10), movmatrix_trans(x11));
         }
         __syncwarp();
         consumed++;
@@ -454,37 +548,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
             cs = 0;
             cphase ^= 1u;
         }
-        if (++csub == (valid + 15) >> 4) {
-            cu++;
-            csub = 0;
-            if (++cslot == spr) {
-                cslot = 0;
-                crow++;
-            }
-        }
-    }
-    if (aborted) {
-        // let the copies already issued land before the CTA's memory is released
-        while (consumed != issued) {
-            mbar_wait_bounded(bar + cs, cphase, kWaitLimitNs);
-            consumed++;
-            if (++cs == S) {
-                cs = 0;
-                cphase ^= 1u;
-            }
-        }
-        return;
+        produce();
     }
     if (cur_row >= 0) finish_row(cur_row);
+    for (int r = empty_from; r <= row_last; r++)
+        if (r != cur_row) write_empty_piece<D>(a, r, gw);
 }
 
 // --------------------------------------------------- fp32 KV, CUDA cores --
 template <int D, bool QF32>
-__global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
     constexpr int PL = D / 32;  // dims per lane: lane + 32 * i
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.group;
-    const int64_t gw = int64_t(blockIdx.x) * kDecodeWarps + warp;
+    const int64_t gw = int64_t(blockIdx.x) * (blockDim.x >> 5) + warp;
     const int64_t u_begin = gw * a.units_per_warp;
     const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
     pdl_trigger();
@@ -578,25 +655,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_simt_kernel(DecodeAr
 template <int D, bool QF32>
 cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
                         cudaStream_t stream) {
+    constexpr int WPC = D == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64;
+    constexpr int HALVES = D == 128 ? kDecodeHalvesD128 : kDecodeHalvesD64;
+    if (grid.warps_per_cta != WPC) return cudaErrorInvalidConfiguration;
     const size_t smem = decode_smem_bytes(D, a.stages);
+    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || configured[dev] < smem) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_bf16_kernel<D, QF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
-    return launch_pdl(decode_bf16_kernel<D, QF32>, dim3(grid.ctas), dim3(kDecodeWarps * 32), smem, stream, *tk, *tv,
-                      a);
+    return launch_pdl(kernel, dim3(grid.ctas), dim3(WPC * 32), smem, stream, *tk, *tv, a);
 }
 
 }  // namespace
 
-// Scratch of qskv_sparse_paged_decode_noalloc: the error word, the per-row
-// merge counters and the split partial outputs live here instead of in a
-// caller-allocated workspace.  Every device that loads the library holds
+// Scratch of qskv_sparse_paged_decode_noalloc: the error word and the split
+// partial outputs live here instead of in a caller-allocated workspace.  Every device that loads the library holds
 // these bytes until the process exits.  All calls share them.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -619,11 +697,14 @@ cudaError_t noalloc_scratch_address(void **ptr) {
     return cudaSuccess;
 }
 
-int decode_stages(int head_dim) { return head_dim == 128 ? 3 : 6; }
+int decode_stages(int head_dim) { return head_dim == 128 ? kDecodeStagesD128 : kDecodeStagesD64; }
+
+int decode_warps_per_cta(int head_dim) { return head_dim == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64; }
 
 size_t decode_smem_bytes(int head_dim, int stages) {
-    const size_t stage = size_t(head_dim / 64) * 16 * 128 * 2;
-    return stage * size_t(stages) * kDecodeWarps + 1024;
+    const int halves = head_dim == 128 ? kDecodeHalvesD128 : kDecodeHalvesD64;
+    const size_t stage = size_t(head_dim / 64) * 16 * 128 * 2 * size_t(halves);  // K and V
+    return stage * size_t(stages) * size_t(decode_warps_per_cta(head_dim)) + 1024;
 }
 
 static cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t stream) {
@@ -647,7 +728,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
         if (e != cudaSuccess) return e;
         return launch_merge(a, head_dim, stream);
     }
-    const dim3 g(grid.ctas), b(kDecodeWarps * 32);
+    const dim3 g(grid.ctas), b(grid.warps_per_cta * 32);
     cudaError_t e;
     if (head_dim == 128)
         e = qf ? launch_pdl(decode_simt_kernel<128, true>, g, b, 0, stream, a)

@@ -14,10 +14,10 @@
 
 namespace qskv {
 
-DecodeGrid decode_grid(int num_sms) {
+DecodeGrid decode_grid(int num_sms, int head_dim) {
     DecodeGrid g;
     g.ctas = kDecodeCtasPerSm * num_sms;
-    g.warps_per_cta = kDecodeWarps;
+    g.warps_per_cta = decode_warps_per_cta(head_dim);
     g.total_warps = int64_t(g.ctas) * g.warps_per_cta;
     return g;
 }
@@ -31,7 +31,7 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
     off += 256;
     w.scores = off;
     off = align256(off + size_t(rows) * size_t(max_pages) * 4);
-    w.slots = rows + decode_grid(num_sms).total_warps;
+    w.slots = rows + decode_grid(num_sms, head_dim).total_warps;
     w.part_o = off;
     off = align256(off + size_t(w.slots) * group * head_dim * 4);
     w.part_lse = off;
@@ -274,7 +274,7 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     const int G = shape->num_q_heads / shape->num_kv_heads;
     const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
     QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
-    const DecodeGrid grid = decode_grid(sms);
+    const DecodeGrid grid = decode_grid(sms, shape->head_dim);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
 
     DecodeArgs a;
@@ -338,7 +338,7 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
     const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
     const int G = shape->num_q_heads / shape->num_kv_heads;
-    const DecodeGrid grid = decode_grid(sms);
+    const DecodeGrid grid = decode_grid(sms, shape->head_dim);
 
     // Layout inside the static scratch: error word, then the partials.
     const int64_t slots = rows + grid.total_warps;

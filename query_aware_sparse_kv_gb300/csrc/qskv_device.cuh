@@ -214,8 +214,23 @@ struct DecodeArgs {
 constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
 constexpr int kSelectThreads = 256;   // ranking CTA: one row
 constexpr int kSelectKeyCap = 4096;   // keys held in shared memory by the select stage
-constexpr int kDecodeWarps = 4;       // warps per decode CTA
 constexpr int kDecodeCtasPerSm = 2;   // decode grid = this x SM count
+// Decode pipeline shape per head dim: warps per CTA, 16-token halves per
+// stage, stages per warp (2 CTAs x warps x stages x stage bytes <= 227 KB).
+#ifndef QSKV_D128_WARPS
+#define QSKV_D128_WARPS 6
+#define QSKV_D128_HALVES 1
+#define QSKV_D128_STAGES 2
+#endif
+#ifndef QSKV_D64_WARPS
+#define QSKV_D64_WARPS 6
+#define QSKV_D64_HALVES 2
+#define QSKV_D64_STAGES 2
+#endif
+constexpr int kDecodeWarpsD128 = QSKV_D128_WARPS, kDecodeHalvesD128 = QSKV_D128_HALVES,
+              kDecodeStagesD128 = QSKV_D128_STAGES;
+constexpr int kDecodeWarpsD64 = QSKV_D64_WARPS, kDecodeHalvesD64 = QSKV_D64_HALVES,
+              kDecodeStagesD64 = QSKV_D64_STAGES;
 constexpr int kMaxStages = 8;
 
 }  // namespace qskv

@@ -32,7 +32,7 @@ struct DecodeGrid {
     int64_t total_warps;
 };
 
-DecodeGrid decode_grid(int num_sms);
+DecodeGrid decode_grid(int num_sms, int head_dim);
 WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms);
 
 cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream);
@@ -49,6 +49,7 @@ cudaError_t noalloc_scratch_address(void **ptr);
 
 // Stage count and dynamic shared memory of the bf16 decode kernel.
 int decode_stages(int head_dim);
+int decode_warps_per_cta(int head_dim);
 size_t decode_smem_bytes(int head_dim, int stages);
 
 }  // namespace qskv
