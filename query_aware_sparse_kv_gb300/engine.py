@@ -66,6 +66,21 @@ class PagedDecoder:
             self.select(q, stream=stream)
         self.decode(q, stream=stream)
 
+    def capture_step(self, q: torch.Tensor, last_ids=None, last_valid=None):
+        """Record one step (metadata refresh, selection, decode) reading the
+        query from the device buffer `q` into a CUDA graph, and return a
+        function that replays it on the current stream.  Refill `q` in place
+        before each replay; results land in ``out`` / ``lse``."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.step(q, last_ids, last_valid)  # first use outside capture (device set-up)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(q, last_ids, last_valid)
+        return graph.replay
+
     def check(self, stream=None):
         """Raise if the device flagged an out-of-range index or a timeout."""
         st = B.get_error(self.workspace, stream)
