@@ -2,8 +2,8 @@
 
 A step is one pass of the whole hot path over one batch: refresh the
 metadata of the page each sequence appends to, select the top-K pages per
-(sequence, KV head), and run sparse paged decode over them (three kernel
-launches).  Inputs are synthetic and resident in HBM (the KV pool exceeds
+(sequence, KV head), and run sparse paged decode over them (three library
+calls, five kernel launches).  Inputs are synthetic and resident in HBM (the KV pool exceeds
 the 129 MB L2, and the query rotates over 16 variants, so a step never finds
 its predecessor's selection in L2).
 
@@ -452,7 +452,8 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step replay",
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
-        "gpu_launches": 3 * args.steps if spec.top_k is not None else 2 * args.steps,
+        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking)
+        "gpu_launches": (5 if spec.top_k is not None else 3) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
