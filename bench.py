@@ -48,12 +48,15 @@ def _es(dtype) -> int:
     return torch.tensor([], dtype=dtype).element_size()
 
 
-def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray | None) -> dict:
+def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray | None,
+               prefix_pages: int = 0) -> dict:
     """Algorithmic bytes of one step, per kernel.
 
     decode: K and V of every 16-token sub-tile holding a valid token of a
             selected page (a whole page when P = 16), q, out, lse, the
-            selected list and one page-table entry per selected page;
+            selected list and one page-table entry per selected page; with
+            a shared prefix of `prefix_pages` pages (cascade decode), the
+            prefix pages once per KV head instead of once per sequence;
     select: the metadata (2 d values) of every page of every row, q, one
             page-table entry per page, the fp32 score written and read back,
             the selected list written;
@@ -75,6 +78,8 @@ def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray
             else:
                 pages = selected[b, g, :int(n_selected[b, g])]
             for j in pages:
+                if b > 0 and int(j) < prefix_pages:
+                    continue  # read once, for the whole batch
                 valid = min(P, int(seq[b]) - int(j) * P)
                 kv += ((valid + 15) // 16) * sub_bytes
                 n_pages_read += 1
@@ -301,7 +306,7 @@ def workload_config(spec: W.Spec) -> dict:
         "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
         "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
         "long_context": "long-context GQA decode, 64K-128K tokens, query-aware top-K paged KV",
-        "shared_prefix": "shared-prefix dense paged decode (all pages)",
+        "shared_prefix": "shared-prefix dense decode (all pages), cascade: prefix once per KV head",
         "tiny": "tiny correctness batch",
     }.get(spec.name, spec.name)
     return {"workload": desc, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
@@ -337,7 +342,8 @@ def run_gpu(args):
     spec = shard_spec(spec, rank)
     inputs = W.make_inputs(spec)
     qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
-    dec = qskv.from_inputs(inputs, device=dev)
+    prefix = spec.prefix_pages if (spec.kind == "shared_prefix" and not args.no_cascade) else 0
+    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix)
     qv = qv_cpu.to(dev)
     ids, vt = W.all_pages(inputs)
     dec.build_meta(ids.to(dev), vt.to(dev))
@@ -353,7 +359,7 @@ def run_gpu(args):
             torch.cuda.synchronize()
             acc.append(step_bytes(inputs, dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy()))
         else:
-            acc.append(step_bytes(inputs, None, None))
+            acc.append(step_bytes(inputs, None, None, prefix_pages=prefix))
             break
     nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
 
@@ -443,7 +449,8 @@ def run_gpu(args):
         "effective_gbs": step_gbs,
         "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
         "bytes_per_step": nbytes,
-        "roofline": {"kernel": "decode_bf16_kernel (qskv_sparse_paged_decode)", "bound": "hbm",
+        "roofline": {"kernel": ("decode_bf16_kernel + prefix_attend_kernel (qskv_cascade_paged_decode)" if prefix
+                                else "decode_bf16_kernel (qskv_sparse_paged_decode)"), "bound": "hbm",
                      "achieved": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": decode_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
                      "decode_ms": decode_ms, "bytes_per_launch": nbytes["decode"],
@@ -452,8 +459,9 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step replay",
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
-        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking)
-        "gpu_launches": (5 if spec.top_k is not None else 3) * args.steps,
+        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking;
+        # cascade: + the shared-prefix kernel)
+        "gpu_launches": (5 if spec.top_k is not None else (4 if prefix else 3)) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -475,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

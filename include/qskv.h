@@ -8,6 +8,12 @@
  *   qskv_sparse_paged_decode softmax(q K^T * scale) V over the selected pages,
  *                            split over warps and merged by log-sum-exp
  *
+ * and a dense decode for batches that share a prefix of pages:
+ *
+ *   qskv_cascade_paged_decode  the shared prefix once per KV head on the
+ *                              tensor cores, each row's own pages paged,
+ *                              merged by log-sum-exp
+ *
  * Sources (web pages on the method):
  *   TinyServe query-aware page selection article: s1 (fixed-size KV pages,
  *   selection per page), s2.1 (metadata m_j, M_j), s2.2 (bound score),
@@ -97,11 +103,10 @@ typedef struct {
  * Bytes of workspace one decode step needs on the current device (the three
  * calls may share one buffer).  The workspace must be 256-byte aligned and
  * zero-filled once before first use (e.g. cudaMemsetAsync); every call
- * leaves it ready for the next one.  It holds the device error word, the
- * per-row completion counters of page selection, a score buffer for callers
- * that pass none, and the split partial outputs of decode (one slot per row
- * plus one per decode warp).  Calls
- * sharing a workspace must not run concurrently on different streams.
+ * leaves it ready for the next one.  It holds the device error word, a
+ * score buffer for callers that pass none, and the split partial outputs of
+ * decode (one slot per row plus one per decode warp).  Calls sharing a
+ * workspace must not run concurrently on different streams.
  * Returns 0 if the shape is invalid or the device cannot be queried.
  */
 size_t qskv_workspace_size(const qskv_shape *shape);
@@ -172,7 +177,7 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
  * workspace.  The split partials and the error word live in an 8 MiB array
  * of device memory built into the library (every GPU that loads the library
  * holds it until the process exits).  A shape whose scratch (about 256 B +
- * (rows + 8 x SM count) x G x (head_dim + 1) x 4 B, rows = batch x
+ * (rows + 12 x SM count) x G x (head_dim + 1) x 4 B, rows = batch x
  * num_kv_heads) exceeds 8 MiB is rejected with QSKV_ERR_WORKSPACE before any
  * launch.  Each call clears the error word with cudaMemsetAsync on `stream`;
  * nothing is allocated or freed.  Device-side index errors still
@@ -188,6 +193,37 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
                                              const int32_t *seq_lens, const qskv_shape *shape,
                                              const int32_t *selected, const int32_t *n_selected, int32_t top_k,
                                              float sm_scale, float *out, float *lse, void *stream);
+
+/*
+ * Shared-prefix cascade decode (prefix sharing: CS336 Lecture 10 s9.2 --
+ * sequences that start alike map their first logical blocks to the same
+ * physical blocks; the attention over a shared anchor and over each
+ * sequence's own suffix merged by log-sum-exp rescaling: Quail AI-SQL engine
+ * article).
+ *
+ * Computes exactly what qskv_sparse_paged_decode computes with selected ==
+ * NULL (dense attention over every token t < seq_len), for a batch whose
+ * rows share their first `prefix_pages` pages: page_table[b][j] ==
+ * page_table[0][j] for every b and every j < prefix_pages, and seq_len >=
+ * prefix_pages * page_size for every b.  The prefix part is computed once
+ * per KV head for all batch x G query rows as a dense product on the
+ * tensor cores (reading the prefix pages once per call, not once per
+ * sequence); each row's own pages j >= prefix_pages go through the paged
+ * decode; the two are merged by log-sum-exp.
+ *   prefix_pages  0 <= prefix_pages <= max_pages (0: plain dense decode)
+ *   workspace     qskv_cascade_workspace_size(shape, prefix_pages) bytes,
+ *                 256-byte aligned, zero-filled once (as for the other calls)
+ * KV must be bf16 (QSKV_ERR_UNSUPPORTED otherwise); q fp32 or bf16.
+ * Device errors: a row that breaks the sharing contract above flags
+ * QSKV_ERR_DEVICE_INDEX (its output is then unspecified, nothing is read out
+ * of bounds); bad page ids are skipped and flagged as in the other calls.
+ */
+size_t qskv_cascade_workspace_size(const qskv_shape *shape, int32_t prefix_pages);
+
+qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
+                                      qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                      const qskv_shape *shape, int32_t prefix_pages, float sm_scale, float *out,
+                                      float *lse, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Synchronises `stream`, reads and clears the workspace's device error flags,

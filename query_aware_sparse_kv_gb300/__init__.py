@@ -6,17 +6,21 @@ in include/qskv.h); this package is its binding:
   kv_meta_build        per-page min/max key metadata
   page_select          bound score of every page and top-K per (sequence, KV head)
   sparse_paged_decode  split-K attention over the selected pages, LSE merge
+  cascade_paged_decode dense decode of a batch sharing a page prefix: the
+                       prefix once per KV head on the tensor cores, the rest
+                       paged, LSE merge
 
 plus ``PagedDecoder`` (buffer plumbing for a whole step) and ``workloads``
 (seeded synthetic inputs).  Nothing here computes on the CPU: without the
 built library every call raises.
 """
-from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, get_error, kv_meta_build,
-                      last_error_message, load, make_shape, page_select, sparse_paged_decode,
-                      sparse_paged_decode_noalloc, workspace_size)
+from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, cascade_paged_decode,
+                      cascade_workspace_size, get_error, kv_meta_build, last_error_message, load, make_shape,
+                      page_select, sparse_paged_decode, sparse_paged_decode_noalloc, workspace_size)
 from .engine import PagedDecoder, from_inputs
 
-__all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "get_error", "kv_meta_build",
+__all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "cascade_paged_decode",
+           "cascade_workspace_size", "get_error", "kv_meta_build",
            "last_error_message", "load", "make_shape", "page_select", "sparse_paged_decode",
            "sparse_paged_decode_noalloc", "workspace_size",
            "PagedDecoder", "from_inputs"]

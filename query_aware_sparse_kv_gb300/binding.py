@@ -23,7 +23,8 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
 
 # Every function the header declares, in declaration order.
 EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_sparse_paged_decode",
-           "qskv_sparse_paged_decode_noalloc", "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
+           "qskv_sparse_paged_decode_noalloc", "qskv_cascade_workspace_size", "qskv_cascade_paged_decode",
+           "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
 
 
 class QskvLibraryMissing(RuntimeError):
@@ -71,6 +72,11 @@ def load(path: str = LIB_PATH):
     lib.qskv_sparse_paged_decode_noalloc.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p,
                                                      i32p, i32, ctypes.c_float, f32p, f32p, vp]
+    lib.qskv_cascade_workspace_size.restype = sz
+    lib.qskv_cascade_workspace_size.argtypes = [sp, i32]
+    lib.qskv_cascade_paged_decode.restype = ctypes.c_int
+    lib.qskv_cascade_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32,
+                                              ctypes.c_float, f32p, f32p, vp, sz, vp]
     lib.qskv_get_error.restype = ctypes.c_int
     lib.qskv_get_error.argtypes = [vp, vp]
     lib.qskv_status_string.restype = ctypes.c_char_p
@@ -160,6 +166,24 @@ def sparse_paged_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: t
                                                    _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape),
                                                    _ptr(selected), _ptr(n_selected), int(top_k), float(sm_scale),
                                                    _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def cascade_workspace_size(shape: Shape, prefix_pages: int) -> int:
+    n = load().qskv_cascade_workspace_size(ctypes.byref(shape), int(prefix_pages))
+    if n == 0:
+        raise QskvError(1, load().qskv_last_error_message().decode())
+    return int(n)
+
+
+def cascade_paged_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor,
+                         seq_lens: torch.Tensor, out: torch.Tensor, shape: Shape, workspace: torch.Tensor,
+                         prefix_pages: int, lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, stream=None):
+    """Dense decode of a batch whose rows share their first `prefix_pages`
+    pages (the workspace must hold cascade_workspace_size bytes)."""
+    _check(load().qskv_cascade_paged_decode(_ptr(q), _dtype(q), _ptr(k_pool), _ptr(v_pool), _dtype(k_pool),
+                                            _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(prefix_pages),
+                                            float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def get_error(workspace: torch.Tensor, stream=None) -> int:

@@ -55,7 +55,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 __device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot) {
     const int b = row / a.num_kv_heads;
     int seq = __ldg(a.seq_lens + b);
-    int ns = 0, j = slot;
+    int ns = 0, j = slot + a.page_begin;
     if (a.selected) {
         ns = __ldg(a.n_selected + row);
         j = __ldg(a.selected + int64_t(row) * a.top_k + slot);
@@ -77,7 +77,7 @@ __device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot)
             raise_error(a.flags, kErrSelected);
             return -1;
         }
-    } else if (slot >= n_b) {
+    } else if (j >= n_b) {
         return -1;
     }
     const int p = __ldg(a.page_table + int64_t(b) * a.max_pages + j);
@@ -96,21 +96,34 @@ __device__ __forceinline__ int unit_code_at(const DecodeArgs &a, int row, int sl
     return unit_code(a, row + dr, s - dr * a.slots_per_row);
 }
 
-// Warps whose unit ranges intersect row `row`.
+// Warps whose unit ranges intersect row `row` (none when there are no units).
 __device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t &w0, int64_t &w1) {
+    if (a.total_units == 0) {
+        w0 = 0;
+        w1 = -1;
+        return;
+    }
     const int64_t first = int64_t(row) * a.slots_per_row;
     const int64_t last = min(first + a.slots_per_row, a.total_units) - 1;
     w0 = first / a.units_per_warp;
     w1 = last / a.units_per_warp;
 }
 
+// A warp that covers a whole row writes the final output itself, unless
+// another kernel contributes pieces to the row.
+__device__ __forceinline__ bool row_is_final(const DecodeArgs &a, int64_t w0, int64_t w1) {
+    return w0 == w1 && a.extra_pieces == 0;
+}
+
 // LSE merge of the split partials (one CTA per row).  Row `row` was split
 // over warps w0..w1; warp w left a normalised partial o_w and its log2-domain
-// log-sum-exp in slot row + w.  out = sum_w 2^(lse_w - m) o_w /
-// sum_w 2^(lse_w - m), lse = m + log2 sum_w 2^(lse_w - m), taken in one pass
-// with a running maximum m; each thread owns one float4 of the row's G x D
-// output and keeps eight slots' loads in flight.  Rows a single warp covered
-// were finished by that warp.
+// log-sum-exp in slot row + w; another kernel may have left extra_pieces more
+// in slots extra_slot0 + row * extra_pieces + e (the shared-prefix part of a
+// cascade decode).  out = sum_w 2^(lse_w - m) o_w / sum_w 2^(lse_w - m),
+// lse = m + log2 sum_w 2^(lse_w - m), taken in one pass with a running
+// maximum m; each thread owns one float4 of the row's G x D output and keeps
+// eight slots' loads in flight.  Rows a single warp covered alone were
+// finished by that warp.
 template <int D>
 __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
     pdl_trigger();
@@ -118,14 +131,17 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
     const int row = blockIdx.x;
     int64_t w0, w1;
     row_warps(a, row, w0, w1);
-    if (w0 == w1) return;
+    if (row_is_final(a, w0, w1)) return;
     constexpr int V4 = D / 4;
     constexpr int SC = 8;
     const int G = a.group;
     const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
-    const int ns = int(w1 - w0 + 1);
-    const float *lse_base = a.part_lse + (row + w0) * G;
-    const float4 *o_base = reinterpret_cast<const float4 *>(a.part_o) + (row + w0) * G * V4;
+    const int nd = int(w1 - w0 + 1);  // pieces from decode warps
+    const int ns = nd + a.extra_pieces;
+    auto slot_of = [&](int j) -> int64_t {
+        return j < nd ? row + w0 + j : a.extra_slot0 + int64_t(row) * a.extra_pieces + (j - nd);
+    };
+    const float4 *o_all = reinterpret_cast<const float4 *>(a.part_o);
     const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
     for (int it = threadIdx.x; it < G * V4; it += blockDim.x) {
         const int h = it / V4, c4 = it % V4;
@@ -137,9 +153,9 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
 #pragma unroll
             for (int j = 0; j < SC; j++) {
                 const bool ok = s0 + j < ns;
-                l[j] = ok ? __ldcg(lse_base + (s0 + j) * G + h) : -INFINITY;
-                v[j] = ok && l[j] != -INFINITY ? __ldcg(o_base + (s0 + j) * G * V4 + it)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                const int64_t sl = ok ? slot_of(s0 + j) : 0;
+                l[j] = ok ? __ldcg(a.part_lse + sl * G + h) : -INFINITY;
+                v[j] = ok && l[j] != -INFINITY ? __ldcg(o_all + sl * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float m = mx;
 #pragma unroll
@@ -180,7 +196,7 @@ __device__ void write_empty_piece(const DecodeArgs &a, int row, int64_t gw) {
     const int G = a.group;
     int64_t w0, w1;
     row_warps(a, row, w0, w1);
-    if (w0 == w1) {
+    if (row_is_final(a, w0, w1)) {
         const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
         const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
         for (int i = lane; i < G * D; i += 32) a.out[qh0 * D + i] = 0.f;
@@ -376,7 +392,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         int64_t w0, w1;
         row_warps(a, row, w0, w1);
         float *dst;
-        if (w0 == w1) {
+        if (row_is_final(a, w0, w1)) {
             const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
             const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G;
             dst = a.out + qh * D;
@@ -589,6 +605,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
     auto finish_row = [&](int row) {
         int64_t w0, w1;
         row_warps(a, row, w0, w1);
+        const bool fin = row_is_final(a, w0, w1);
         const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
         const int64_t qh = int64_t(b) * a.num_q_heads + int64_t(g) * G;
         const int64_t slot = row + gw;
@@ -597,11 +614,11 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
             if (h >= G) break;
             const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
             const float e = l[h] > 0.f ? m[h] + log2f(l[h]) : -INFINITY;
-            float *dst = (w0 == w1) ? a.out + (qh + h) * D : a.part_o + (slot * G + h) * D;
+            float *dst = fin ? a.out + (qh + h) * D : a.part_o + (slot * G + h) * D;
 #pragma unroll
             for (int i = 0; i < PL; i++) dst[lane + 32 * i] = o[h][i] * inv;
             if (lane == 0) {
-                if (w0 == w1) {
+                if (fin) {
                     if (a.lse) a.lse[qh + h] = e * kLn2;
                 } else {
                     a.part_lse[slot * G + h] = e;
@@ -714,9 +731,28 @@ static cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t 
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
-                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream) {
-    if (a.total_units == 0) return cudaSuccess;
+                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream,
+                          const PrefixArgs *prefix) {
     const bool qf = q_dtype == kDtypeF32;
+    if (prefix) {
+        // cascade: the rows' own pages, then the shared prefix (which may
+        // start on SMs the decode grid's last CTAs leave), then the merge
+        cudaError_t e = cudaSuccess;
+        if (a.total_units > 0) {
+            if (kv_dtype != kDtypeBf16) return cudaErrorInvalidValue;
+            if (head_dim == 128)
+                e = qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
+                       : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
+            else
+                e = qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
+                       : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+            if (e != cudaSuccess) return e;
+        }
+        e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
+        if (e != cudaSuccess) return e;
+        return launch_merge(a, head_dim, stream);
+    }
+    if (a.total_units == 0) return cudaSuccess;
     if (kv_dtype == kDtypeBf16) {
         cudaError_t e;
         if (head_dim == 128)

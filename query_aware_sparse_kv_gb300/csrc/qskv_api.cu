@@ -24,14 +24,15 @@ DecodeGrid decode_grid(int num_sms, int head_dim) {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms) {
+WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms,
+                                 int extra_per_row) {
     WorkspaceLayout w;
     size_t off = 0;
     w.flags = off;
     off += 256;
     w.scores = off;
     off = align256(off + size_t(rows) * size_t(max_pages) * 4);
-    w.slots = rows + decode_grid(num_sms, head_dim).total_warps;
+    w.slots = rows + decode_grid(num_sms, head_dim).total_warps + rows * extra_per_row;
     w.part_o = off;
     off = align256(off + size_t(w.slots) * group * head_dim * 4);
     w.part_lse = off;
@@ -299,6 +300,9 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     a.num_pool_pages = shape->num_pool_pages;
     a.top_k = selected ? top_k : 0;
     a.slots_per_row = selected ? top_k : shape->max_pages;
+    a.page_begin = 0;
+    a.extra_pieces = 0;
+    a.extra_slot0 = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -381,6 +385,9 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     a.num_pool_pages = shape->num_pool_pages;
     a.top_k = selected ? top_k : 0;
     a.slots_per_row = selected ? top_k : shape->max_pages;
+    a.page_begin = 0;
+    a.extra_pieces = 0;
+    a.extra_slot0 = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -396,6 +403,110 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     }
     return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, st),
                     "sparse_paged_decode_noalloc launch");
+}
+
+size_t qskv_cascade_workspace_size(const qskv_shape *shape, int32_t prefix_pages) {
+    if (check_shape(shape) != QSKV_OK) return 0;
+    if (prefix_pages < 0 || prefix_pages > shape->max_pages) {
+        fail(QSKV_ERR_INVALID_ARG, "prefix_pages must be in [0, max_pages] (got %d)", prefix_pages);
+        return 0;
+    }
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) {
+        fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+        return 0;
+    }
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const int E = prefix_splits(shape->batch, G, shape->num_kv_heads, shape->page_size, prefix_pages, sms);
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    return workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms, E).total;
+}
+
+qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
+                                      qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                      const qskv_shape *shape, int32_t prefix_pages, float sm_scale, float *out,
+                                      float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (kv_dtype != QSKV_BF16) return fail(QSKV_ERR_UNSUPPORTED, "the cascade decode needs a bf16 KV cache");
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out)
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool, page_table, seq_lens and out must be non-NULL");
+    if (prefix_pages < 0 || prefix_pages > shape->max_pages)
+        return fail(QSKV_ERR_INVALID_ARG, "prefix_pages must be in [0, max_pages] (got %d)", prefix_pages);
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool and out must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and lse arrays must be 4-byte aligned");
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return fail(QSKV_ERR_INVALID_ARG, "sm_scale must be finite and >= 0");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const int E = prefix_splits(shape->batch, G, shape->num_kv_heads, shape->page_size, prefix_pages, sms);
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms, E);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    const DecodeGrid grid = decode_grid(sms, shape->head_dim);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
+
+    DecodeArgs a;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = nullptr;
+    a.n_selected = nullptr;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float *>(ws + L.part_o);
+    a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = 0;
+    a.page_begin = E > 0 ? prefix_pages : 0;
+    a.slots_per_row = shape->max_pages - a.page_begin;
+    a.extra_pieces = E;
+    a.extra_slot0 = rows + grid.total_warps;
+    a.stages = decode_stages(shape->head_dim);
+    a.total_units = rows * a.slots_per_row;
+    a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    PrefixArgs p;
+    p.q = q;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.part_o = a.part_o;
+    p.part_lse = a.part_lse;
+    p.flags = a.flags;
+    p.batch = shape->batch;
+    p.num_q_heads = shape->num_q_heads;
+    p.num_kv_heads = shape->num_kv_heads;
+    p.group = G;
+    p.page_size = shape->page_size;
+    p.max_pages = shape->max_pages;
+    p.num_pool_pages = shape->num_pool_pages;
+    p.prefix_pages = prefix_pages;
+    p.splits = E;
+    p.slot0 = a.extra_slot0;
+    p.scale_log2 = a.scale_log2;
+
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    QSKV_TRY(make_pool_map(&tk, k_pool, shape));
+    QSKV_TRY(make_pool_map(&tv, v_pool, shape));
+    return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid,
+                                  static_cast<cudaStream_t>(stream), E > 0 ? &p : nullptr),
+                    "cascade_paged_decode launch");
 }
 
 qskv_status qskv_get_error(void *workspace, void *stream) {
@@ -414,6 +525,7 @@ qskv_status qskv_get_error(void *workspace, void *stream) {
     if (flags & kErrSeqLen) what += " seq_len-out-of-range";
     if (flags & kErrValid) what += " valid-tokens-out-of-range";
     if (flags & kErrTimeout) what += " wait-timeout";
+    if (flags & kErrPrefix) what += " shared-prefix-contract-broken";
     if (flags & kErrTimeout) return fail(QSKV_ERR_DEVICE_TIMEOUT, "device flags:%s", what.c_str());
     return fail(QSKV_ERR_DEVICE_INDEX, "device flags:%s", what.c_str());
 }

@@ -18,6 +18,7 @@ enum : uint32_t {
     kErrSeqLen = 4u,    // seq_len < 0 or > max_pages * page_size
     kErrValid = 8u,     // valid-token count outside [1, page_size]
     kErrTimeout = 16u,  // a bounded mbarrier wait gave up
+    kErrPrefix = 32u,   // a row breaks the shared-prefix contract of the cascade decode
 };
 
 // A wait on a TMA transfer that has not completed after this long is treated
@@ -60,6 +61,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Waits for the phase with the given parity to complete; false after limit_ns.
@@ -117,6 +122,92 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------ tcgen05 tensor cores --
+// One CTA (cta_group::1).  Tensor memory (TMEM) is 128 lanes x 512 columns
+// of 32 bits per SM; an address is lane << 16 | column.  Warp w of a CTA may
+// read and write lanes 32 (w % 4) .. 32 (w % 4) + 31 only.
+
+// Allocates `ncols` TMEM columns (a power of two >= 32) for the CTA and
+// stores the base address at `dst`.  Executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Frees an allocation; executed by the warp that made it, after every
+// tensor-core operation on it has completed.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations against thread synchronisation (mbarrier or
+// bar.sync): "before" ahead of the signalling side, "after" behind the
+// waiting side.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Instruction descriptor of a dense kind::f16 MMA with bf16 A and B and an
+// fp32 accumulator: M x N tile, A / B either K-major or MN-major in shared
+// memory.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                         // D: fp32
+           | (1u << 7) | (1u << 10)          // A, B: bf16
+           | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+           (uint32_t(N >> 3) << 17)          // N / 8
+           | (uint32_t(M >> 4) << 24);       // M / 16
+}
+
+// Shared-memory matrix descriptor for the 128-byte swizzled layout (rows of
+// 128 bytes, 8-row / 1024-byte swizzle atoms whose base is 1024-aligned).
+// K-major operand: `sbo` = bytes between 8-row groups, `lbo` unused.
+// MN-major operand: `lbo` = bytes between 64-element groups along M/N,
+// `sbo` = bytes between 8-row groups along K.
+__device__ __forceinline__ uint64_t tc_sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46)  // descriptor version
+           | (uint64_t(2) << 61);                                          // 128-byte swizzle
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, issued by one thread.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+        : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05 operation this thread issued
+// before it has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive columns of this thread's TMEM lane -> registers, waited
+// for before returning.  Warp-collective.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Registers -> 32 consecutive columns of this thread's TMEM lane, waited for
+// before returning.  Warp-collective.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 // ------------------------------------------------------ warp matrix ops --
@@ -204,12 +295,36 @@ struct DecodeArgs {
     float *part_lse;        // [slots][G], log2 domain
     uint32_t *flags;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages, top_k;
-    int32_t slots_per_row;  // top_k (sparse) or max_pages (dense)
+    int32_t slots_per_row;  // top_k (sparse) or max_pages - page_begin (dense)
+    int32_t page_begin;     // dense: slot s is logical page page_begin + s
+    int32_t extra_pieces;   // partials per row written by another kernel (0: none)
+    int64_t extra_slot0;    // row r's extra piece e sits in slot extra_slot0 + r * extra_pieces + e
     int32_t stages;
     int64_t total_units;    // rows * slots_per_row
     int64_t units_per_warp; // ceil(total_units / total_warps)
     float scale_log2;       // sm_scale * log2(e)
 };
+
+// Shared-prefix cascade: the attention of all B x G query rows of one KV head
+// over the shared prefix, one CTA per (128-row tile, KV head, key split).
+struct PrefixArgs {
+    const void *q;          // [B][Hq][D]
+    const int32_t *page_table;
+    const int32_t *seq_lens;
+    float *part_o;          // [slots][G][D]
+    float *part_lse;        // [slots][G], log2 domain
+    uint32_t *flags;
+    int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages;
+    int32_t prefix_pages;   // logical pages [0, prefix_pages) are shared by every row
+    int32_t splits;         // key splits per (tile, head)
+    int64_t slot0;          // row r's split s writes slot slot0 + r * splits + s
+    float scale_log2;
+};
+
+constexpr int kPrefixRows = 128;      // query rows per prefix CTA (the MMA's M)
+constexpr int kPrefixKeys = 128;      // keys per prefix block (the S tile's N)
+constexpr int kPrefixThreads = 192;   // 4 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kMaxPrefixSplits = 64;
 
 constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
 constexpr int kSelectThreads = 256;   // ranking CTA: one row

@@ -14,6 +14,7 @@ constexpr int kDtypeBf16 = 1; // matches QSKV_BF16
 struct MetaArgs;
 struct SelectArgs;
 struct DecodeArgs;
+struct PrefixArgs;
 
 // Workspace layout: every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
@@ -22,7 +23,7 @@ struct WorkspaceLayout {
     size_t part_o;       // fp32  [slots][G][D]
     size_t part_lse;     // fp32  [slots][G]
     size_t total;
-    int64_t slots;       // rows + decode warps
+    int64_t slots;       // rows + decode warps (+ rows x prefix splits)
 };
 
 // Decode grid shape on a device with `num_sms` SMs.
@@ -33,15 +34,28 @@ struct DecodeGrid {
 };
 
 DecodeGrid decode_grid(int num_sms, int head_dim);
-WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms);
+// extra_per_row: partial slots per row for the shared-prefix pieces of a
+// cascade decode (0 otherwise).
+WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms,
+                                 int extra_per_row = 0);
 
 cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream);
 // score_all: compute scores even for rows where every page is kept.
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
                                int score_all);
-// tmap_k / tmap_v are used by the bf16 tensor-core kernel only.
+// tmap_k / tmap_v are used by the bf16 tensor-core kernels only.  With
+// `prefix` (a cascade decode, bf16 KV) the shared-prefix kernel runs between
+// the decode and the merge.
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
-                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream);
+                          int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream,
+                          const PrefixArgs *prefix = nullptr);
+// Shared-prefix attention of a cascade decode: 128-row query tiles per KV
+// head, and the key splits per (tile, head) chosen for a device with
+// `num_sms` SMs (0 when the prefix is empty).
+int prefix_tiles(int batch, int group);
+int prefix_splits(int batch, int group, int num_kv_heads, int page_size, int prefix_pages, int num_sms);
+cudaError_t launch_prefix(const PrefixArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
+                          int head_dim, cudaStream_t stream);
 // Size of the static device scratch used by qskv_sparse_paged_decode_noalloc
 // and its device address on the current device (looked up on first use).
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;

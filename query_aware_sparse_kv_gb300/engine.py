@@ -22,9 +22,13 @@ class PagedDecoder:
     page_table  [batch][max_pages] int32  physical page ids
     seq_lens    [batch] int32
     top_k       pages kept per (sequence, KV head); None = dense decode
+    prefix_pages  logical pages [0, prefix_pages) every row shares (the same
+                physical pages): dense decodes then run as a cascade, the
+                prefix attended once per KV head for the whole batch
     """
 
-    def __init__(self, q, k_pool, v_pool, page_table, seq_lens, top_k: Optional[int], sm_scale: float = 0.0):
+    def __init__(self, q, k_pool, v_pool, page_table, seq_lens, top_k: Optional[int], sm_scale: float = 0.0,
+                 prefix_pages: int = 0):
         dev = k_pool.device
         self.q, self.k_pool, self.v_pool = q, k_pool, v_pool
         self.page_table, self.seq_lens = page_table, seq_lens
@@ -33,8 +37,12 @@ class PagedDecoder:
         self.top_k = top_k
         self.sm_scale = sm_scale
         self.shape = B.make_shape(batch, hq, hkv, d, P, page_table.shape[1], n_pool)
+        self.prefix_pages = int(prefix_pages)
         self.meta = torch.empty((n_pool, hkv, 2, d), dtype=k_pool.dtype, device=dev)
-        self.workspace = torch.zeros(B.workspace_size(self.shape), dtype=torch.uint8, device=dev)
+        ws = B.workspace_size(self.shape)
+        if self.prefix_pages > 0:
+            ws = max(ws, B.cascade_workspace_size(self.shape, self.prefix_pages))
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
         k = max(int(top_k or 1), 1)
         self.selected = torch.full((batch, hkv, k), -1, dtype=torch.int32, device=dev)
         self.n_selected = torch.zeros((batch, hkv), dtype=torch.int32, device=dev)
@@ -52,6 +60,12 @@ class PagedDecoder:
 
     def decode(self, q=None, dense: bool = False, out=None, lse=None, stream=None):
         sel = None if (dense or self.top_k is None) else self.selected
+        if sel is None and self.prefix_pages > 0:
+            B.cascade_paged_decode(self.q if q is None else q, self.k_pool, self.v_pool, self.page_table,
+                                   self.seq_lens, self.out if out is None else out, self.shape, self.workspace,
+                                   self.prefix_pages, lse=self.lse if lse is None else lse, sm_scale=self.sm_scale,
+                                   stream=stream)
+            return
         B.sparse_paged_decode(self.q if q is None else q, self.k_pool, self.v_pool, self.page_table, self.seq_lens,
                               self.out if out is None else out, self.shape, self.workspace, selected=sel,
                               n_selected=self.n_selected if sel is not None else None,
@@ -88,9 +102,10 @@ class PagedDecoder:
             raise B.QskvError(st, B.last_error_message())
 
 
-def from_inputs(inputs: dict, device="cuda", top_k="spec") -> PagedDecoder:
+def from_inputs(inputs: dict, device="cuda", top_k="spec", prefix_pages: int = 0) -> PagedDecoder:
     """A PagedDecoder over a workloads.make_inputs() batch copied to `device`."""
     if isinstance(top_k, str):
         top_k = inputs["top_k"]
     t = {k: inputs[k].to(device) for k in ("q", "k_pool", "v_pool", "page_table", "seq_lens")}
-    return PagedDecoder(t["q"], t["k_pool"], t["v_pool"], t["page_table"], t["seq_lens"], top_k)
+    return PagedDecoder(t["q"], t["k_pool"], t["v_pool"], t["page_table"], t["seq_lens"], top_k,
+                        prefix_pages=prefix_pages)

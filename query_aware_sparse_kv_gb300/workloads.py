@@ -19,7 +19,9 @@ are used):
 * ``long_context``   -- 4 sequences of U[65536, 131072] tokens, page 32,
                         keys drawn around 64 centroids, q near one of them.
 * ``shared_prefix``  -- 256 sequences sharing 128 aliased prefix pages plus
-                        32 private pages each; dense (all pages).
+                        32 private pages each; dense (all pages).  With
+                        ``seq_lens`` given, each sequence holds the prefix
+                        and ceil(seq_len / P) - prefix_pages private pages.
 
 Slots of a partially filled last page hold NaN in K and V: every consumer
 must ignore tokens at or beyond ``seq_len``.
@@ -96,6 +98,10 @@ def spec_for(name: str, **overrides) -> Spec:
 def _draw_seq_lens(spec: Spec, g: torch.Generator) -> torch.Tensor:
     if spec.kind == "shared_prefix":
         n = (spec.prefix_pages + spec.suffix_pages) * spec.page_size
+        if spec.seq_lens is not None:
+            assert len(spec.seq_lens) == spec.batch
+            assert all(spec.prefix_pages * spec.page_size <= x <= n for x in spec.seq_lens)
+            return torch.tensor(list(spec.seq_lens), dtype=torch.int32)
         return torch.full((spec.batch,), n, dtype=torch.int32)
     if spec.seq_lens is not None:
         assert len(spec.seq_lens) == spec.batch
@@ -137,7 +143,8 @@ def make_inputs(spec: Spec) -> dict:
         for b in range(B):
             table[b, :spec.prefix_pages] = perm[:spec.prefix_pages]
             s0 = spec.prefix_pages + b * spec.suffix_pages
-            table[b, spec.prefix_pages:spec.prefix_pages + spec.suffix_pages] = perm[s0:s0 + spec.suffix_pages]
+            own = int(n_pages[b]) - spec.prefix_pages
+            table[b, spec.prefix_pages:spec.prefix_pages + own] = perm[s0:s0 + own]
     else:
         total = int(n_pages.sum())
         n_pool = total + spec.extra_pool_pages

@@ -27,7 +27,7 @@ def _declared():
 
 def test_header_declares_the_three_calls():
     names = _declared()
-    for n in ("qskv_kv_meta_build", "qskv_page_select", "qskv_sparse_paged_decode"):
+    for n in ("qskv_kv_meta_build", "qskv_page_select", "qskv_sparse_paged_decode", "qskv_cascade_paged_decode"):
         assert n in names
     assert sorted(binding.EXPORTS) == names
 
@@ -94,6 +94,28 @@ def test_argument_checks(lib):
     assert lib.qskv_kv_meta_build(p, 1, ctypes.byref(shape), p, p, -1, p, p, 4096, None) == 1
     assert lib.qskv_kv_meta_build(p, 1, ctypes.byref(shape), p, p, 1, p, ctypes.c_void_p(base + 8), 4096, None) == 3
     assert lib.qskv_kv_meta_build(p, 1, ctypes.byref(shape), p, p, 0, p, p, 4096, None) == 0
+
+
+def test_cascade_argument_checks(lib):
+    shape = qskv.make_shape(2, 8, 2, 128, 16, 8, 16)
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+
+    def call(q=p, kv_dtype=1, prefix=4, out=p, scale=0.0, shp=shape):
+        return lib.qskv_cascade_paged_decode(q, 1, p, p, kv_dtype, p, p, ctypes.byref(shp), prefix, scale, out, None,
+                                             p, 4096, None)
+
+    assert call(kv_dtype=0) == 2          # fp32 KV cache
+    assert call(q=None) == 1              # NULL query
+    assert call(prefix=-1) == 1           # prefix outside [0, max_pages]
+    assert call(prefix=9) == 1
+    assert call(out=ctypes.c_void_p(base + 4)) == 1  # misaligned output
+    assert call(scale=-2.0) == 1
+    assert call(shp=qskv.make_shape(2, 8, 2, 96, 16, 8, 16)) == 2  # head_dim 96
+    assert lib.qskv_last_error_message().decode()
+    assert lib.qskv_cascade_workspace_size(ctypes.byref(shape), -1) == 0
+    assert lib.qskv_cascade_workspace_size(ctypes.byref(shape), 9) == 0
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):

@@ -39,3 +39,12 @@ def test_dense_counts_every_page():
     nb = bench.step_bytes(inp, None, None)
     assert nb["kv"] == 3 * 8 * 3 * 16 * 128 * 2 * 2
     assert nb["select"] == 0
+
+
+def test_cascade_counts_the_prefix_once():
+    """3 sequences x 8 KV heads share 2 prefix pages and own 1 page each:
+    the cascade reads (2 + 3 x 1) page-heads of K and V per KV head."""
+    spec = W.spec_for("shared_prefix", batch=3, prefix_pages=2, suffix_pages=1)
+    inp = W.make_inputs(spec)
+    nb = bench.step_bytes(inp, None, None, prefix_pages=2)
+    assert nb["kv"] == 8 * (2 + 3 * 1) * 16 * 128 * 2 * 2
