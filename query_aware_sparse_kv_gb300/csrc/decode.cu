@@ -136,49 +136,51 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
     constexpr int SC = 8;
     const int G = a.group;
     const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
-    const int nd = int(w1 - w0 + 1);  // pieces from decode warps
-    const int ns = nd + a.extra_pieces;
-    auto slot_of = [&](int j) -> int64_t {
-        return j < nd ? row + w0 + j : a.extra_slot0 + int64_t(row) * a.extra_pieces + (j - nd);
-    };
+    const int nd = int(w1 - w0 + 1);  // pieces from decode warps: slots row + w0 ..
+    const int ne = a.extra_pieces;    // pieces from another kernel: slots extra_slot0 + row * ne ..
+    const int64_t slot_d = row + w0, slot_e = a.extra_slot0 + int64_t(row) * ne;
     const float4 *o_all = reinterpret_cast<const float4 *>(a.part_o);
     const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
     for (int it = threadIdx.x; it < G * V4; it += blockDim.x) {
         const int h = it / V4, c4 = it % V4;
         float mx = -INFINITY, den = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < ns; s0 += SC) {
-            float l[SC];
-            float4 v[SC];
+        // folds n consecutive slots into (mx, den, acc)
+        auto fold = [&](const float *lse_p, const float4 *o_p, int n) {
+            for (int s0 = 0; s0 < n; s0 += SC) {
+                float l[SC];
+                float4 v[SC];
 #pragma unroll
-            for (int j = 0; j < SC; j++) {
-                const bool ok = s0 + j < ns;
-                const int64_t sl = ok ? slot_of(s0 + j) : 0;
-                l[j] = ok ? __ldcg(a.part_lse + sl * G + h) : -INFINITY;
-                v[j] = ok && l[j] != -INFINITY ? __ldcg(o_all + sl * G * V4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < SC; j++) {
+                    const bool ok = s0 + j < n;
+                    l[j] = ok ? __ldcg(lse_p + (s0 + j) * G) : -INFINITY;
+                    v[j] = ok && l[j] != -INFINITY ? __ldcg(o_p + (s0 + j) * G * V4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                float m = mx;
+#pragma unroll
+                for (int j = 0; j < SC; j++) m = fmaxf(m, l[j]);
+                if (m == -INFINITY) continue;
+                const float sc = exp2f(mx - m);
+                den *= sc;
+                acc.x *= sc;
+                acc.y *= sc;
+                acc.z *= sc;
+                acc.w *= sc;
+#pragma unroll
+                for (int j = 0; j < SC; j++) {
+                    if (l[j] == -INFINITY) continue;  // an empty piece: its o was never written
+                    const float w = exp2f(l[j] - m);
+                    den += w;
+                    acc.x = fmaf(w, v[j].x, acc.x);
+                    acc.y = fmaf(w, v[j].y, acc.y);
+                    acc.z = fmaf(w, v[j].z, acc.z);
+                    acc.w = fmaf(w, v[j].w, acc.w);
+                }
+                mx = m;
             }
-            float m = mx;
-#pragma unroll
-            for (int j = 0; j < SC; j++) m = fmaxf(m, l[j]);
-            if (m == -INFINITY) continue;
-            const float sc = exp2f(mx - m);
-            den *= sc;
-            acc.x *= sc;
-            acc.y *= sc;
-            acc.z *= sc;
-            acc.w *= sc;
-#pragma unroll
-            for (int j = 0; j < SC; j++) {
-                if (l[j] == -INFINITY) continue;  // an empty piece: its o was never written
-                const float w = exp2f(l[j] - m);
-                den += w;
-                acc.x = fmaf(w, v[j].x, acc.x);
-                acc.y = fmaf(w, v[j].y, acc.y);
-                acc.z = fmaf(w, v[j].z, acc.z);
-                acc.w = fmaf(w, v[j].w, acc.w);
-            }
-            mx = m;
-        }
+        };
+        fold(a.part_lse + slot_d * G + h, o_all + slot_d * G * V4 + it, nd);
+        if (ne > 0) fold(a.part_lse + slot_e * G + h, o_all + slot_e * G * V4 + it, ne);
         const float inv = den > 0.f ? 1.f / den : 0.f;
         reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -232,7 +234,10 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     const int64_t u_begin = gw * a.units_per_warp;
     const int64_t u_end = min(u_begin + a.units_per_warp, a.total_units);
     pdl_trigger();
-    if (u_begin >= u_end) return;
+    if (u_begin >= u_end) {
+        if (a.wait_at_exit) pdl_wait();
+        return;
+    }
 
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) +
                     size_t(warp) * S * STAGE;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         prefetch_tensormap(&tmap_v);
     }
     __syncwarp();
-    pdl_wait();
+    if (!a.wait_at_exit) pdl_wait();
 
     // Units are walked with (row, slot) cursors, never by dividing the
     // 64-bit unit index in the loop.
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                     cphase ^= 1u;
                 }
             }
+            if (a.wait_at_exit) pdl_wait();
             return;
         }
         const int row = __shfl_sync(0xffffffffu, st_row, cs);
@@ -569,6 +575,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     if (cur_row >= 0) finish_row(cur_row);
     for (int r = empty_from; r <= row_last; r++)
         if (r != cur_row) write_empty_piece<D>(a, r, gw);
+    if (a.wait_at_exit) pdl_wait();
 }
 
 // --------------------------------------------------- fp32 KV, CUDA cores --
@@ -735,21 +742,25 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
                           const PrefixArgs *prefix) {
     const bool qf = q_dtype == kDtypeF32;
     if (prefix) {
-        // cascade: the rows' own pages, then the shared prefix (which may
-        // start on SMs the decode grid's last CTAs leave), then the merge
-        cudaError_t e = cudaSuccess;
+        // cascade: the shared prefix first; it waits for the previous kernel
+        // and then releases the decode of the rows' own pages, which runs on
+        // the SMs the prefix grid leaves free and, in its place, as prefix
+        // CTAs finish.  The decode waits for the prefix grid only at its
+        // exit, so the merge behind it sees both.
+        if (kv_dtype != kDtypeBf16) return cudaErrorInvalidValue;
+        cudaError_t e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
+        if (e != cudaSuccess) return e;
         if (a.total_units > 0) {
-            if (kv_dtype != kDtypeBf16) return cudaErrorInvalidValue;
+            DecodeArgs d = a;
+            d.wait_at_exit = 1;
             if (head_dim == 128)
-                e = qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
-                       : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
+                e = qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream)
+                       : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream);
             else
-                e = qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
-                       : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+                e = qf ? launch_bf16<64, true>(d, tmap_k, tmap_v, grid, stream)
+                       : launch_bf16<64, false>(d, tmap_k, tmap_v, grid, stream);
             if (e != cudaSuccess) return e;
         }
-        e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
-        if (e != cudaSuccess) return e;
         return launch_merge(a, head_dim, stream);
     }
     if (a.total_units == 0) return cudaSuccess;

@@ -15,45 +15,59 @@
 // A CTA owns one tile of 128 query rows (row = sequence-major, query head of
 // the group minor), one KV head and one contiguous range of 128-key blocks
 // of the prefix (a key split).  Roles:
-//   warp 4, TMA:   gathers each block's pages (K and V, 16-token x 64-dim
-//                  boxes, 128-byte swizzle) into a two-stage ring;
-//   warp 5, MMA:   one lane issues S = Q . K^T into tensor memory (two S
+//   TMA warps:     one for K, one for V.  Each gathers its blocks' pages
+//                  (16-token x 64-dim boxes, 128-byte swizzle) into its own
+//                  ring, deep enough to cover the load latency (a K stage is
+//                  refilled as soon as its Q . K^T has run, a V stage once
+//                  its P . V has); page ids are read one ring-round ahead.
+//   MMA warp:      one lane issues S = Q . K^T into tensor memory (two S
 //                  buffers, so S of block j+1 is computed while block j's
-//                  softmax runs) and O += P . V into a TMEM accumulator;
-//   warps 0-3:     thread r owns query row r (TMEM lane r): it reads its S
-//                  row, keeps the online-softmax state (exp2 with the scale
-//                  folded into log2 e; the running maximum is only moved, and
-//                  O rescaled in TMEM, when a block's maximum exceeds it by
-//                  more than 2^8), writes its bf16 P row into shared memory
-//                  for the next MMA, and at the end normalises its O row into
-//                  the workspace slot of (row, split) with its log2-domain
-//                  log-sum-exp.
-// fp32 queries are split into bf16 hi + lo tiles (two MMAs per k-step).  The
-// softmax denominator sums the same bf16-rounded probabilities the P . V
-// product uses.  Every wait is bounded; a wait that gives up flags a timeout,
-// stops the CTA's other roles, lets issued copies and MMAs complete and frees
-// the tensor memory before the CTA exits.
+//                  softmax runs), then O += P . V into a TMEM accumulator,
+//                  with P (and, for bf16 queries, Q) read from tensor memory.
+//   softmax warps: two threads per query row (TMEM lane), each owning 64 of
+//                  a block's keys and half of the output dims.  A thread
+//                  reads its S columns, takes its partial maximum and keeps
+//                  the online-softmax state (exp2 with the scale folded into
+//                  log2 e, a partial denominator summing the same bf16 values
+//                  P . V uses).  The running maximum only moves when a
+//                  block's maximum exceeds it by more than 2^8 (one barrier
+//                  vote per block; the partial maxima are exchanged only then,
+//                  or for the first block), and O is then rescaled in TMEM.
+//                  The bf16 P pairs go to a TMEM region of their own once the
+//                  previous block's P . V has completed.  At the end each
+//                  thread normalises its part of the O row into the workspace
+//                  slot of (row, split); the log2-domain log-sum-exp goes with it.
+// fp32 queries are split into bf16 hi + lo tiles kept in shared memory (two
+// MMAs per k-step).  Every wait is bounded; a wait that gives up flags a
+// timeout, stops the CTA's other roles, lets issued copies and MMAs complete
+// and frees the tensor memory before the CTA exits.
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
 
 namespace qskv {
 namespace {
 
+constexpr int kPrefixMaxStages = 6;
+
 template <int D, bool QF32>
 struct PrefixCfg {
     static constexpr int NB = D / 64;                 // 64-dim (128-byte) column groups
     static constexpr int ATOM = 128 * 128;            // 128 rows x 128 bytes
-    static constexpr int QB = NB * ATOM;              // one 128-row Q tile
-    static constexpr int NQ = QF32 ? 2 : 1;           // hi (+ lo) tiles
+    static constexpr bool Q_TMEM = !QF32;             // bf16 Q: A operand from tensor memory
+    static constexpr int QB = NB * ATOM;              // one 128-row Q tile in shared memory
+    static constexpr int QSMEM = QF32 ? 2 * QB : 0;   // fp32 Q: hi + lo tiles
     static constexpr int KVB = NB * ATOM;             // K (or V) of one 128-key block
-    static constexpr int NSTAGE = 2;
-    static constexpr int NP = (QF32 && D == 128) ? 1 : 2;  // P buffers
-    static constexpr int PB = 2 * ATOM;               // 128 rows x 128 keys
-    static constexpr int SMEM = NQ * QB + NSTAGE * 2 * KVB + NP * PB + 1024;
+    // ring depths: the K and V rings fill what shared memory is left
+    static constexpr int NK = QF32 ? (D == 128 ? 2 : 5) : (D == 128 ? 4 : 6);
+    static constexpr int NV = QF32 ? (D == 128 ? 2 : 5) : (D == 128 ? 3 : 6);
+    static constexpr int SMEM = QSMEM + (NK + NV) * KVB + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;              // S buffers: columns [0, 256)
-    static constexpr uint32_t O_COL = 256;            // O: columns [256, 256 + D)
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t O_COL = 256;            // O: [256, 256 + D)
+    static constexpr uint32_t P_COL = 384;            // P as bf16 pairs: [384, 448)
+    static constexpr uint32_t Q_COL = 448;            // bf16 Q pairs: [448, 448 + D/2)
+    static_assert(NK <= kPrefixMaxStages && NV <= kPrefixMaxStages, "ring depth");
+    static_assert(SMEM + 2048 <= 227 * 1024, "shared memory budget (dynamic + static)");
 };
 
 // Bounded wait that also gives up when another role of the CTA has.
@@ -74,18 +88,31 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
 
 // The cascade's contract for the sequences of tile `mt`: their first
 // prefix_pages table entries equal row 0's and they hold the whole prefix.
-__device__ void check_prefix_contract(const PrefixArgs &a, int mt, int r, int T) {
+__device__ void check_prefix_contract(const PrefixArgs &a, int mt, int t, int nthreads, int T) {
     const int G = a.group;
     const int b_first = mt * (kPrefixRows / G);
     const int b_end = min(a.batch, b_first + kPrefixRows / G);
     const int nseq = b_end - b_first;
     bool bad = false;
-    for (int idx = r; idx < nseq * a.prefix_pages; idx += kPrefixRows) {
+    for (int idx = t; idx < nseq * a.prefix_pages; idx += nthreads) {
         const int bb = b_first + idx / a.prefix_pages, jj = idx % a.prefix_pages;
         bad |= __ldg(a.page_table + int64_t(bb) * a.max_pages + jj) != __ldg(a.page_table + jj);
     }
-    for (int bb = b_first + r; bb < b_end; bb += kPrefixRows) bad |= __ldg(a.seq_lens + bb) < T;
+    for (int bb = b_first + t; bb < b_end; bb += nthreads) bad |= __ldg(a.seq_lens + bb) < T;
     if (bad) raise_error(a.flags, kErrPrefix);
+}
+
+// Page id of lane `lane`'s page in block `blk` (lanes >= pages in the block,
+// and invalid ids, give -1; invalid ids are flagged).
+__device__ __forceinline__ int block_page_id(const PrefixArgs &a, int blk, int ppb, int lane) {
+    const int pg = blk * ppb + lane;
+    if (lane >= ppb || pg >= a.prefix_pages) return -1;
+    const int pid = __ldg(a.page_table + pg);  // row 0's entries name the shared pages
+    if (pid < 0 || pid >= a.num_pool_pages) {
+        raise_error(a.flags, kErrPageId);
+        return -1;
+    }
+    return pid;
 }
 
 template <int D, bool QF32>
@@ -95,11 +122,21 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     using C = PrefixCfg<D, QF32>;
     constexpr int ATOM = C::ATOM;
     constexpr int KEYS = kPrefixKeys;
+    constexpr int TPR = kPrefixRowThreads;
+    constexpr int SW = 4 * TPR;           // softmax warps
+    constexpr int NSM = 32 * SW;          // softmax threads
+    constexpr int KP = KEYS / TPR;        // keys of a block per softmax thread
+    constexpr int DP = D / TPR;           // output dims per softmax thread
+    constexpr int MMA_WARP = SW, K_WARP = SW + 1, V_WARP = SW + 2;
+    constexpr uint32_t kBarRows = 1;      // named barrier of the softmax threads
     constexpr float kLazy = 8.f;
+    static_assert(KP % 32 == 0 && DP % 32 == 0, "a thread moves whole 32-column TMEM groups");
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s_full[2], bar_s_free[2],
-        bar_p_full[2], bar_p_free[2], bar_o_full, bar_drain;
+    __shared__ __align__(8) uint64_t bar_q, bar_k_full[kPrefixMaxStages], bar_k_empty[kPrefixMaxStages],
+        bar_v_full[kPrefixMaxStages], bar_v_empty[kPrefixMaxStages], bar_s_full[2], bar_s_free[2], bar_p_full,
+        bar_pv_done, bar_o_full, bar_drain;
+    __shared__ float red[TPR][kPrefixRows];
     __shared__ uint32_t s_tmem;
     __shared__ volatile uint32_t s_abort;
 
@@ -114,30 +151,38 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     const int nblk = (T + KEYS - 1) / KEYS;
     const int blk0 = int(int64_t(split) * nblk / a.splits);
     const int nloc = int(int64_t(split + 1) * nblk / a.splits) - blk0;  // >= 1: splits <= nblk
+    // Everything before this grid in the stream has completed before the
+    // dependents (the decode of the rows' own pages) are released: they
+    // skip their own wait until exit.
+    pdl_wait();
     pdl_trigger();
 
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *q_s = base;                           // [NQ][NB][128 rows][128 B]
-    uint8_t *kv_s = base + C::NQ * C::QB;          // stage st: K at + st*2*KVB, V at + KVB
-    uint8_t *p_s = kv_s + C::NSTAGE * 2 * C::KVB;  // [NP][2][128 rows][128 B]
+    uint8_t *q_s = base;                        // fp32 Q: [2][NB][128 rows][128 B]
+    uint8_t *k_s = base + C::QSMEM;             // [NK][NB][128 keys][128 B]
+    uint8_t *v_s = k_s + C::NK * C::KVB;        // [NV][NB][128 keys][128 B]
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar_q, 128);
-        for (int i = 0; i < 2; i++) {
-            mbar_init(&bar_kv_full[i], 1);
-            mbar_init(&bar_kv_empty[i], 1);
-            mbar_init(&bar_s_full[i], 1);
-            mbar_init(&bar_s_free[i], 128);
-            mbar_init(&bar_p_full[i], 128);
-            mbar_init(&bar_p_free[i], 1);
+        mbar_init(&bar_q, NSM);
+        for (int i = 0; i < kPrefixMaxStages; i++) {
+            mbar_init(&bar_k_full[i], 1);
+            mbar_init(&bar_k_empty[i], 1);
+            mbar_init(&bar_v_full[i], 1);
+            mbar_init(&bar_v_empty[i], 1);
         }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&bar_s_full[i], 1);
+            mbar_init(&bar_s_free[i], NSM);
+        }
+        mbar_init(&bar_p_full, NSM);
+        mbar_init(&bar_pv_done, 1);
         mbar_init(&bar_o_full, 1);
         mbar_init(&bar_drain, 1);
         s_abort = 0u;
         mbar_fence_init();
     }
-    if (warp == 5) tmem_alloc(&s_tmem, C::TMEM_COLS);
-    if (warp == 4 && lane == 0) {
+    if (warp == MMA_WARP) tmem_alloc(&s_tmem, C::TMEM_COLS);
+    if (warp == K_WARP && lane == 0) {
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
@@ -146,21 +191,47 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp < 4) {
+    if (warp < SW) {
         // ------------------------------------------------ softmax rows
-        const int r = threadIdx.x;
+        const int quarter = warp & 3, part = warp >> 2;
+        const int r = quarter * 32 + lane;  // tile row = TMEM lane
         const int tr = mt * kPrefixRows + r;
         const int b = tr / G, hq = tr % G;
         const bool row_ok = b < a.batch;
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const uint32_t lane_base = uint32_t(quarter * 32) << 16;
         {
             const int64_t qoff = (int64_t(row_ok ? b : 0) * a.num_q_heads + int64_t(g) * G + hq) * D;
-#pragma unroll 4
-            for (int ch = 0; ch < D / 8; ch++) {  // 16-byte chunks of 8 dims
-                uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
-                if (row_ok) {
-                    if (QF32) {
-                        const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + qoff) + 2 * ch;
+            if (C::Q_TMEM) {
+                // bf16 pairs of the row into TMEM lane r; with d = 64 one
+                // thread of the row stores all 32 columns
+                constexpr int QC = D / 2;                    // columns of a Q row
+                constexpr int QT = QC / TPR >= 32 ? QC / TPR : QC;
+                if (QT == QC / TPR || part == 0) {
+                    const int c0 = QT == QC ? 0 : part * QT;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff);
+#pragma unroll
+                    for (int cb = 0; cb < QT / 32; cb++) {
+                        uint32_t rr[32];
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            const uint4 v = row_ok ? __ldg(src + (c0 + cb * 32) / 4 + k) : make_uint4(0, 0, 0, 0);
+                            rr[4 * k] = v.x;
+                            rr[4 * k + 1] = v.y;
+                            rr[4 * k + 2] = v.z;
+                            rr[4 * k + 3] = v.w;
+                        }
+                        tmem_st32(tmem + lane_base + C::Q_COL + c0 + cb * 32, rr);
+                    }
+                }
+                tc_fence_before();
+            } else {
+                constexpr int CH = D / 8 / TPR;  // 16-byte chunks of 8 dims per thread
+#pragma unroll
+                for (int ch = part * CH; ch < (part + 1) * CH; ch++) {
+                    uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
+                    if (row_ok) {
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + qoff) + 2 * ch;
                         const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
                         hv = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
                                         pack_bf16x2(x1.z, x1.w));
@@ -168,102 +239,120 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                                         pack_bf16x2(x0.z - bf16_lo_to_float(hv.y), x0.w - bf16_hi_to_float(hv.y)),
                                         pack_bf16x2(x1.x - bf16_lo_to_float(hv.z), x1.y - bf16_hi_to_float(hv.z)),
                                         pack_bf16x2(x1.z - bf16_lo_to_float(hv.w), x1.w - bf16_hi_to_float(hv.w)));
-                    } else {
-                        hv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff) + ch);
                     }
+                    const uint32_t off = (ch >> 3) * ATOM + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(q_s + off) = hv;
+                    *reinterpret_cast<uint4 *>(q_s + C::QB + off) = lv;
                 }
-                const uint32_t off = (ch >> 3) * ATOM + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(q_s + off) = hv;
-                if (QF32) *reinterpret_cast<uint4 *>(q_s + C::QB + off) = lv;
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             mbar_arrive(&bar_q);
         }
-        if (g == 0 && split == 0) check_prefix_contract(a, mt, r, T);
+        if (g == 0 && split == 0) check_prefix_contract(a, mt, threadIdx.x, NSM, T);
 
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
+        const float sc = a.scale_log2;
+        float m = -INFINITY;  // running maximum of the scaled logits (log2 domain)
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // partial denominator over this thread's keys
+        bool ok = true;       // warp-uniform; after a failed wait the warp only keeps
+                              // visiting the named barriers (they have no time limit)
         for (int i = 0; i < nloc; i++) {
             const int ntok = min(KEYS, T - (blk0 + i) * KEYS);
-            const int sb = i & 1, pb = i % C::NP;
-            ok = __all_sync(0xffffffffu, wait_phase(&bar_s_full[sb], (i >> 1) & 1, &s_abort, a.flags));
-            if (!ok) break;
-            tc_fence_after();
-            float sv[KEYS];
+            const int sb = i & 1;
+            float sv[KP];
+            float lmax = -INFINITY;
+            if (ok) ok = __all_sync(0xffffffffu, wait_phase(&bar_s_full[sb], (i >> 1) & 1, &s_abort, a.flags));
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < KEYS / 32; cb++) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_base + C::S_COL + sb * KEYS + cb * 32, rr);
+                for (int cb = 0; cb < KP / 32; cb++) {
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + lane_base + C::S_COL + sb * KEYS + part * KP + cb * 32, rr);
 #pragma unroll
-                for (int k = 0; k < 32; k++) sv[cb * 32 + k] = __uint_as_float(rr[k]);
+                    for (int k = 0; k < 32; k++) sv[cb * 32 + k] = __uint_as_float(rr[k]);
+                }
+                tc_fence_before();
+                mbar_arrive(&bar_s_free[sb]);
+                if (ntok < KEYS) {
+#pragma unroll
+                    for (int k = 0; k < KP; k++)
+                        if (part * KP + k >= ntok) sv[k] = -INFINITY;
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int k = 0; k < KP; k++) mx[k & 3] = fmaxf(mx[k & 3], sv[k]);
+                lmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             }
-            tc_fence_before();
-            mbar_arrive(&bar_s_free[sb]);
-            float bm = -INFINITY;
+            // the row's maximum is needed on the first block, and later only
+            // when some row's block maximum leaves the 2^8 band
+            float mn = m;
+            if (i == 0 || named_bar_any(kBarRows, NSM, ok && lmax * sc > m + kLazy)) {
+                red[part][r] = lmax;
+                named_bar_sync(kBarRows, NSM);
+                float rm = red[0][r];
 #pragma unroll
-            for (int k = 0; k < KEYS; k++) {
-                const float x = k < ntok ? sv[k] * a.scale_log2 : -INFINITY;
-                sv[k] = x;
-                bm = fmaxf(bm, x);
+                for (int pp = 1; pp < TPR; pp++) rm = fmaxf(rm, red[pp][r]);
+                const float cand = rm * sc;
+                mn = (i == 0 || cand > m + kLazy) ? cand : m;
+                named_bar_sync(kBarRows, NSM);  // everyone has read `red` before it is reused
             }
-            if (i == 0) {
-                m = bm;  // O is written (not accumulated) by the first P . V
-            } else {
-                const bool resc = bm > m + kLazy;
-                if (__any_sync(0xffffffffu, resc)) {
-                    // P . V of the previous block must have landed in O first
-                    const int pp = i - 1;
-                    ok = __all_sync(0xffffffffu,
-                                    wait_phase(&bar_p_free[pp % C::NP], (pp / C::NP) & 1, &s_abort, a.flags));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const float mn = resc ? bm : m;
-                    const float al = exp2f(m - mn);
+            if (!ok) continue;
+            uint32_t pk[KP / 2];
+#pragma unroll
+            for (int k = 0; k < KP / 2; k++) {
+                pk[k] = pack_bf16x2(exp2f(fmaf(sv[2 * k], sc, -mn)), exp2f(fmaf(sv[2 * k + 1], sc, -mn)));
+            }
+            const float al = exp2f(m - mn);  // 1 for rows that keep their maximum
+#pragma unroll
+            for (int k = 0; k < 4; k++) l4[k] *= al;
+#pragma unroll
+            for (int k = 0; k < KP / 2; k++)
+                l4[k & 3] += bf16_lo_to_float(pk[k]) + bf16_hi_to_float(pk[k]);
+            if (i > 0) {
+                // P . V of the previous block must be complete: it read the
+                // P region and accumulated into O
+                ok = __all_sync(0xffffffffu, wait_phase(&bar_pv_done, (i - 1) & 1, &s_abort, a.flags));
+                if (!ok) continue;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, mn != m)) {
 #pragma unroll 1
-                    for (int cb = 0; cb < D / 32; cb++) {
+                    for (int cb = 0; cb < DP / 32; cb++) {
                         uint32_t rr[32];
-                        const uint32_t ta = tmem + lane_base + C::O_COL + cb * 32;
+                        const uint32_t ta = tmem + lane_base + C::O_COL + part * DP + cb * 32;
                         tmem_ld32(ta, rr);
 #pragma unroll
                         for (int k = 0; k < 32; k++) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * al);
                         tmem_st32(ta, rr);
                     }
-                    l *= al;
-                    m = mn;
                 }
             }
-            if (i >= C::NP) {  // P buffer pb is free once P . V of block i - NP completed
-                ok = __all_sync(0xffffffffu,
-                                wait_phase(&bar_p_free[pb], ((i - C::NP) / C::NP) & 1, &s_abort, a.flags));
-                if (!ok) break;
-            }
-            uint8_t *prow = p_s + pb * C::PB + r * 128;
+            m = mn;
 #pragma unroll
-            for (int ch = 0; ch < KEYS / 8; ch++) {
-                uint32_t w[4];
+            for (int cb = 0; cb < KP / 64; cb++) {
+                uint32_t rr[32];
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    w[k] = pack_bf16x2(exp2f(sv[ch * 8 + 2 * k] - m), exp2f(sv[ch * 8 + 2 * k + 1] - m));
-                    l += bf16_lo_to_float(w[k]) + bf16_hi_to_float(w[k]);
-                }
-                *reinterpret_cast<uint4 *>(prow + (ch >> 3) * ATOM + (((ch & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+                for (int k = 0; k < 32; k++) rr[k] = pk[cb * 32 + k];
+                tmem_st32(tmem + lane_base + C::P_COL + part * (KP / 2) + cb * 32, rr);
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar_p_full[pb]);
+            mbar_arrive(&bar_p_full);
         }
+        // the row's denominator: the parts' partial sums (all softmax threads
+        // take part, whatever happened above)
+        red[part][r] = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        named_bar_sync(kBarRows, NSM);
+        float l = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < TPR; pp++) l += red[pp][r];
         if (ok) ok = __all_sync(0xffffffffu, wait_phase(&bar_o_full, 0, &s_abort, a.flags));
         if (ok) {
             tc_fence_after();
-            pdl_wait();  // the previous user of the workspace slots has finished
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t slot = a.slot0 + (int64_t(row_ok ? b : 0) * a.num_kv_heads + g) * a.splits + split;
-            float4 *dst = reinterpret_cast<float4 *>(a.part_o + (slot * G + hq) * D);
+            float4 *dst = reinterpret_cast<float4 *>(a.part_o + (slot * G + hq) * D + part * DP);
 #pragma unroll 1
-            for (int cb = 0; cb < D / 32; cb++) {
+            for (int cb = 0; cb < DP / 32; cb++) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_base + C::O_COL + cb * 32, rr);
+                tmem_ld32(tmem + lane_base + C::O_COL + part * DP + cb * 32, rr);
                 if (row_ok) {
 #pragma unroll
                     for (int k = 0; k < 8; k++)
@@ -272,105 +361,127 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                                                       __uint_as_float(rr[4 * k + 3]) * inv);
                 }
             }
-            if (row_ok) a.part_lse[slot * G + hq] = l > 0.f ? m + log2f(l) : -INFINITY;
+            if (row_ok && part == 0) a.part_lse[slot * G + hq] = l > 0.f ? m + log2f(l) : -INFINITY;
         }
-    } else if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+    } else if (warp == K_WARP || warp == V_WARP) {
+        // ------------------------------------------------ TMA producers
+        const bool is_k = warp == K_WARP;
+        const int NS = is_k ? C::NK : C::NV;
+        const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+        const uint8_t *pool = static_cast<const uint8_t *>(is_k ? a.k_pool : a.v_pool);
+        uint8_t *ring = is_k ? k_s : v_s;
+        uint64_t *full = is_k ? bar_k_full : bar_v_full;
+        uint64_t *empty = is_k ? bar_k_empty : bar_v_empty;
         const int ppb = KEYS / P;  // pages per block
+        const uint32_t tile_bytes = uint32_t(P) * D * 2;
+        // every page tile of this key range, requested from L2 up front (by
+        // the first query tile's CTA only: the others read the same pages)
+        for (int idx = lane; mt == 0 && idx < nloc * ppb; idx += 32) {
+            const int pg = blk0 * ppb + idx;
+            if (pg < a.prefix_pages) {
+                const int pid = __ldg(a.page_table + pg);
+                if (pid >= 0 && pid < a.num_pool_pages)
+                    prefetch_l2_bulk(pool + (int64_t(pid) * a.num_kv_heads + g) * tile_bytes, tile_bytes);
+            }
+        }
+        // page ids of the next ring-round of blocks, lane j holding page j
+        int ids[kPrefixMaxStages];
+#pragma unroll
+        for (int s = 0; s < kPrefixMaxStages; s++)
+            ids[s] = s < NS && s < nloc ? block_page_id(a, blk0 + s, ppb, lane) : -1;
         int nissued = 0;
         bool ok = true;
         for (int i = 0; i < nloc; i++) {
-            const int st = i % C::NSTAGE;
-            if (i >= C::NSTAGE) {
-                ok = __all_sync(0xffffffffu,
-                                wait_phase(&bar_kv_empty[st], ((i / C::NSTAGE) - 1) & 1, &s_abort, a.flags));
+            const int st = i % NS;
+            int pid = -1;
+#pragma unroll
+            for (int s = 0; s < kPrefixMaxStages; s++)
+                if (s == st) pid = ids[s];
+            if (i >= NS) {
+                ok = __all_sync(0xffffffffu, wait_phase(&empty[st], ((i / NS) - 1) & 1, &s_abort, a.flags));
                 if (!ok) break;
             }
-            uint8_t *ks = kv_s + st * 2 * C::KVB, *vs = ks + C::KVB;
-            const int pg0 = (blk0 + i) * ppb;
-            const int npg = min(ppb, a.prefix_pages - pg0);
-            int pid = -1;
-            if (lane < npg) {
-                pid = __ldg(a.page_table + pg0 + lane);  // row 0's entries name the shared pages
-                if (pid < 0 || pid >= a.num_pool_pages) {
-                    raise_error(a.flags, kErrPageId);
-                    pid = -1;
-                }
-            }
+            uint8_t *buf = ring + st * C::KVB;
             const uint32_t good = __ballot_sync(0xffffffffu, pid >= 0);
             if (good != (1u << ppb) - 1u) {
                 // token rows without data (past the prefix, or an invalid
-                // page): zero K and V so the masked columns stay finite
+                // page) are zeroed so the masked columns stay finite
                 for (int idx = lane; idx < KEYS * C::NB * 8; idx += 32) {
                     const int row = idx / (C::NB * 8), rest = idx % (C::NB * 8);
                     if ((good >> (row / P)) & 1u) continue;
-                    const uint32_t off = (rest >> 3) * ATOM + row * 128 + (rest & 7) * 16;
-                    *reinterpret_cast<uint4 *>(ks + off) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(vs + off) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(buf + (rest >> 3) * ATOM + row * 128 + (rest & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&bar_kv_full[st], uint32_t(__popc(good)) * P * D * 2 * 2);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(__popc(good)) * tile_bytes);
             __syncwarp();
             if (pid >= 0) {
                 for (int sub = 0; sub < P / 16; sub++) {
                     const int y = (pid * a.num_kv_heads + g) * P + sub * 16;
                     const int row = lane * P + sub * 16;
 #pragma unroll
-                    for (int nb = 0; nb < C::NB; nb++) {
-                        tma_load_2d(ks + nb * ATOM + row * 128, &tmap_k, nb * 64, y, &bar_kv_full[st]);
-                        tma_load_2d(vs + nb * ATOM + row * 128, &tmap_v, nb * 64, y, &bar_kv_full[st]);
-                    }
+                    for (int nb = 0; nb < C::NB; nb++) tma_load_2d(buf + nb * ATOM + row * 128, map, nb * 64, y, &full[st]);
                 }
             }
             nissued++;
+            // this stage's next block: its ids are read now, a ring-round ahead
+            const int nxt = i + NS < nloc ? block_page_id(a, blk0 + i + NS, ppb, lane) : -1;
+#pragma unroll
+            for (int s = 0; s < kPrefixMaxStages; s++)
+                if (s == st) ids[s] = nxt;
         }
         if (!ok) {  // copies already issued land before the CTA's memory is released
-            for (int i = max(0, nissued - C::NSTAGE); i < nissued; i++)
-                mbar_wait_bounded(&bar_kv_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, kWaitLimitNs);
+            for (int i = max(0, nissued - NS); i < nissued; i++)
+                mbar_wait_bounded(&full[i % NS], (i / NS) & 1, kWaitLimitNs);
         }
     } else {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = tc_idesc_bf16(128, KEYS, false, false);
             constexpr uint32_t idO = tc_idesc_bf16(128, D, false, true);
-            const uint32_t qa = smem_u32(q_s), kva = smem_u32(kv_s), pa0 = smem_u32(p_s);
+            const uint32_t qa = smem_u32(q_s), ka0 = smem_u32(k_s), va0 = smem_u32(v_s);
             bool issued = false;
             auto pv = [&](int i) -> bool {
-                const int pb = i % C::NP, st = i % C::NSTAGE;
-                if (!wait_phase(&bar_p_full[pb], (i / C::NP) & 1, &s_abort, a.flags)) return false;
+                const int st = i % C::NV;
+                if (!wait_phase(&bar_p_full, i & 1, &s_abort, a.flags)) return false;
+                if (!wait_phase(&bar_v_full[st], (i / C::NV) & 1, &s_abort, a.flags)) return false;
                 tc_fence_after();
-                const uint32_t pa = pa0 + pb * C::PB, va = kva + st * 2 * C::KVB + C::KVB;
+                const uint32_t va = va0 + st * C::KVB;
 #pragma unroll
                 for (int ks = 0; ks < KEYS / 16; ks++) {
-                    // A = P (K-major, keys along K); B = V (MN-major: dims contiguous)
-                    const uint64_t ad = tc_sdesc_sw128(pa + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = tc_sdesc_sw128(va + ks * 16 * 128, ATOM, 1024);
-                    tc_mma_bf16(tmem + C::O_COL, ad, bd, idO, i > 0 || ks > 0);
+                    // A = P from TMEM (8 columns = 16 keys); B = V, MN-major (dims contiguous)
+                    tc_mma_bf16_ts(tmem + C::O_COL, tmem + C::P_COL + ks * 8,
+                                   tc_sdesc_sw128(va + ks * 16 * 128, ATOM, 1024), idO, i > 0 || ks > 0);
                 }
-                tc_commit(&bar_kv_empty[st]);
-                tc_commit(&bar_p_free[pb]);
+                tc_commit(&bar_v_empty[st]);
+                tc_commit(&bar_pv_done);
                 return true;
             };
             bool ok = wait_phase(&bar_q, 0, &s_abort, a.flags);
             for (int i = 0; i < nloc && ok; i++) {
-                const int st = i % C::NSTAGE, sb = i & 1;
-                ok = wait_phase(&bar_kv_full[st], (i / C::NSTAGE) & 1, &s_abort, a.flags);
+                const int st = i % C::NK, sb = i & 1;
+                ok = wait_phase(&bar_k_full[st], (i / C::NK) & 1, &s_abort, a.flags);
                 if (ok && i >= 2) ok = wait_phase(&bar_s_free[sb], ((i - 2) >> 1) & 1, &s_abort, a.flags);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t ka = kva + st * 2 * C::KVB;
+                const uint32_t ka = ka0 + st * C::KVB;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
-                    // A = Q, B = K, both K-major (dims contiguous)
+                    // A = Q (TMEM, or K-major in shared memory), B = K, K-major
                     const uint32_t koff = (kk >> 2) * ATOM + (kk & 3) * 32;
                     const uint64_t bd = tc_sdesc_sw128(ka + koff, 16, 1024);
-                    tc_mma_bf16(tmem + C::S_COL + sb * KEYS, tc_sdesc_sw128(qa + koff, 16, 1024), bd, idS, kk > 0);
-                    if (QF32)
-                        tc_mma_bf16(tmem + C::S_COL + sb * KEYS, tc_sdesc_sw128(qa + C::QB + koff, 16, 1024), bd, idS,
-                                    true);
+                    if (C::Q_TMEM) {
+                        tc_mma_bf16_ts(tmem + C::S_COL + sb * KEYS, tmem + C::Q_COL + kk * 8, bd, idS, kk > 0);
+                    } else {
+                        tc_mma_bf16(tmem + C::S_COL + sb * KEYS, tc_sdesc_sw128(qa + koff, 16, 1024), bd, idS,
+                                    kk > 0);
+                        tc_mma_bf16(tmem + C::S_COL + sb * KEYS, tc_sdesc_sw128(qa + C::QB + koff, 16, 1024), bd,
+                                    idS, true);
+                    }
                 }
+                tc_commit(&bar_k_empty[st]);
                 tc_commit(&bar_s_full[sb]);
                 issued = true;
                 if (i >= 1) ok = pv(i - 1);
@@ -387,7 +498,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }

@@ -303,6 +303,7 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     a.page_begin = 0;
     a.extra_pieces = 0;
     a.extra_slot0 = 0;
+    a.wait_at_exit = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -388,6 +389,7 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     a.page_begin = 0;
     a.extra_pieces = 0;
     a.extra_slot0 = 0;
+    a.wait_at_exit = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -475,6 +477,7 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     a.slots_per_row = shape->max_pages - a.page_begin;
     a.extra_pieces = E;
     a.extra_slot0 = rows + grid.total_warps;
+    a.wait_at_exit = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -482,6 +485,8 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
 
     PrefixArgs p;
     p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
     p.page_table = page_table;
     p.seq_lens = seq_lens;
     p.part_o = a.part_o;

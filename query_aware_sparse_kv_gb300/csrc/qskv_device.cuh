@@ -120,6 +120,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned global address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -182,6 +188,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]^T, issued by one thread: A is M x 16 bf16
+// elements held in TMEM lanes 0..M-1, two per 32-bit column, K-ascending.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+        : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
@@ -208,6 +226,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns whether `pred` held on any participant.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // ------------------------------------------------------ warp matrix ops --
@@ -299,6 +336,9 @@ struct DecodeArgs {
     int32_t page_begin;     // dense: slot s is logical page page_begin + s
     int32_t extra_pieces;   // partials per row written by another kernel (0: none)
     int64_t extra_slot0;    // row r's extra piece e sits in slot extra_slot0 + r * extra_pieces + e
+    int32_t wait_at_exit;   // 1: wait for the previous grid at exit, not before the first access
+                            // (the previous grid is the cascade's prefix kernel, which itself
+                            // waited for everything before it)
     int32_t stages;
     int64_t total_units;    // rows * slots_per_row
     int64_t units_per_warp; // ceil(total_units / total_warps)
@@ -309,6 +349,8 @@ struct DecodeArgs {
 // over the shared prefix, one CTA per (128-row tile, KV head, key split).
 struct PrefixArgs {
     const void *q;          // [B][Hq][D]
+    const void *k_pool;     // [Npool][Hkv][P][D] bf16 (for L2 prefetch; loads go through the tensor maps)
+    const void *v_pool;
     const int32_t *page_table;
     const int32_t *seq_lens;
     float *part_o;          // [slots][G][D]
@@ -323,7 +365,8 @@ struct PrefixArgs {
 
 constexpr int kPrefixRows = 128;      // query rows per prefix CTA (the MMA's M)
 constexpr int kPrefixKeys = 128;      // keys per prefix block (the S tile's N)
-constexpr int kPrefixThreads = 192;   // 4 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kPrefixRowThreads = 2;  // softmax threads per query row (each owns 64 of a block's keys)
+constexpr int kPrefixThreads = 128 * kPrefixRowThreads + 96;  // softmax warps, MMA warp, K and V TMA warps
 constexpr int kMaxPrefixSplits = 64;
 
 constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
