@@ -11,7 +11,9 @@ Every function states the passage it follows:
   attention over only those pages;
   CS336 Lecture 10 "Inference" -- s2.3 decode attention, s9.2 PagedAttention
   block tables and shared prefixes;
-  Quail AI-SQL engine article -- partial attention merged by log-sum-exp.
+  Quail AI-SQL engine article -- partial attention merged by log-sum-exp;
+  Vortex sparse-attention digest, method overview item 1 -- per-block mean
+  keys ("centroids") from the cache phase, Block Top-K scoring q . centroid.
 """
 
 from __future__ import annotations
@@ -57,6 +59,12 @@ def _load():
         lib.orc_row_scores.restype = ctypes.c_int
         lib.orc_row_scores.argtypes = [_f64p, ctypes.c_int, _f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, _i32p, ctypes.c_int, _f64p]
+        lib.orc_centroid.restype = ctypes.c_int
+        lib.orc_centroid.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _i32p, _i32p, ctypes.c_int64, _f64p]
+        lib.orc_centroid_scores.restype = ctypes.c_int
+        lib.orc_centroid_scores.argtypes = [_f64p, ctypes.c_int, _f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, _i32p, ctypes.c_int, _f64p]
         lib.orc_select.restype = ctypes.c_int
         lib.orc_select.argtypes = [_f64p, ctypes.c_int, ctypes.c_int, _i32p]
         lib.orc_attend_row.restype = ctypes.c_int
@@ -67,7 +75,8 @@ def _load():
         lib.orc_set_threads.restype = ctypes.c_int
         lib.orc_set_threads.argtypes = [ctypes.c_int]
         lib.orc_step.restype = ctypes.c_int
-        lib.orc_step.argtypes = [_f64p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, _f64p, _i32p, _i32p,
+        lib.orc_step.argtypes = [_f64p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, _f64p, ctypes.c_int,
+                                 _i32p, _i32p,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_double, _i32p,
                                  ctypes.c_int, _i32p, _i32p, _f64p, _f64p, _f64p]
@@ -136,6 +145,39 @@ def row_scores(q_group, meta_arr: np.ndarray, table_row, n_b: int, g: int) -> np
     return out[:n_b]
 
 
+def centroids(k_pool: torch.Tensor, page_ids, valid_tokens, out: np.ndarray | None = None) -> np.ndarray:
+    """Vortex item 1 (cache phase): per-(page, KV head) mean of the valid keys.
+
+    Returns float64 [Npool][Hkv][d]; pages not listed are NaN (or keep
+    ``out``'s values)."""
+    lib = _load()
+    n_pool, hkv, P, d = k_pool.shape
+    if out is None:
+        out = np.full((n_pool, hkv, d), np.nan)
+    ids, vt = _i32(page_ids), _i32(valid_tokens)
+    ptr, dt = _pool(k_pool)
+    rc = lib.orc_centroid(ptr, dt, n_pool, hkv, P, d, _p(ids, _i32p), _p(vt, _i32p), len(ids), _p(out, _f64p))
+    if rc != 0:
+        raise IndexError("oracle centroids: page id or valid-token count out of range")
+    return out
+
+
+def centroid_row_scores(q_group, cent: np.ndarray, table_row, n_b: int, g: int) -> np.ndarray:
+    """Vortex item 1 (indexer phase, Block Top-K): S(j) = max over the group's
+    heads of q_h . centroid of page j, j < n_b."""
+    qg = _f64(q_group)
+    G, d = qg.shape
+    n_pool, hkv = cent.shape[:2]
+    tr = _i32(table_row)
+    out = np.empty(max(n_b, 1))
+    _load().orc_centroid_scores(_p(qg, _f64p), G, _p(cent, _f64p), n_pool, hkv, g, d, _p(tr, _i32p), n_b,
+                                _p(out, _f64p))
+    return out[:n_b]
+
+
+SCORERS = {"bound": 0, "centroid": 1}
+
+
 def select(scores, top_k: int) -> tuple[np.ndarray, int]:
     """TinyServe s2.3: top_k pages by score (ties -> lower index), ascending, -1 padded."""
     s = _f64(scores)
@@ -171,11 +213,13 @@ def attend_row(inputs: dict, b: int, g: int, pages, sm_scale: float | None = Non
 
 
 def step(inputs: dict, rows=None, top_k: int | None = "spec", meta_arr: np.ndarray | None = None,
-         sm_scale: float | None = None, q=None, threads: int | None = None) -> dict:
+         sm_scale: float | None = None, q=None, threads: int | None = None, scorer: str = "bound") -> dict:
     """One full decode step (scores -> top-K -> attention) over ``rows``
     (row = b * Hkv + g; default all).  ``top_k=None`` (or a dense spec) means
-    every page.  Returns numpy arrays keyed selected, n_sel, scores, out, lse,
-    plus the OpenMP thread count used."""
+    every page.  ``scorer`` is "bound" (TinyServe s2.2, meta_arr = min/max
+    rows) or "centroid" (Vortex Block Top-K, meta_arr = centroids).  Returns
+    numpy arrays keyed selected, n_sel, scores, out, lse, plus the OpenMP
+    thread count used."""
     spec = inputs["spec"]
     if isinstance(top_k, str):
         top_k = spec.top_k
@@ -190,7 +234,7 @@ def step(inputs: dict, rows=None, top_k: int | None = "spec", meta_arr: np.ndarr
     dense = top_k is None or top_k <= 0
     if not dense and meta_arr is None:
         ids, vt = _all_pages(inputs)
-        meta_arr = meta(inputs["k_pool"], ids, vt)
+        meta_arr = (centroids if scorer == "centroid" else meta)(inputs["k_pool"], ids, vt)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
     qd = _f64(inputs["q"] if q is None else q)
@@ -208,7 +252,8 @@ def step(inputs: dict, rows=None, top_k: int | None = "spec", meta_arr: np.ndarr
     lib = _load()
     if threads is not None:
         lib.orc_set_threads(int(threads))
-    nthr = lib.orc_step(_p(qd, _f64p), kp, vp, dt, meta_p, _p(table, _i32p), _p(sl, _i32p), B, Hq, Hkv, d, P,
+    nthr = lib.orc_step(_p(qd, _f64p), kp, vp, dt, meta_p, SCORERS[scorer], _p(table, _i32p), _p(sl, _i32p), B,
+                        Hq, Hkv, d, P,
                         max_pages, n_pool, kk, sm_scale, _p(rows, _i32p), n_rows, _p(selected, _i32p),
                         _p(n_sel, _i32p), _p(scores, _f64p) if scores is not None else None, _p(out, _f64p),
                         _p(lse, _f64p))

@@ -19,6 +19,11 @@
  *   [QU]  Quail AI-SQL engine article, section "the inference engine as an
  *         execution engine" (partial attention results combined by
  *         log-sum-exp rescaling, as in flash decoding).
+ *   [VX]  Vortex sparse-attention digest, method overview item 1: a
+ *         query-independent cache phase computes per-block summaries such as
+ *         the block's mean key ("centroids"); the query-dependent indexer
+ *         phase scores each block from q and its summary, keeps the top-K
+ *         blocks and attends over them ("Block Top-K").
  *
  * Readings taken where the pages are silent (listed with the design notes):
  *   - the comparator lost in the extracted formula is "q[i] > 0";
@@ -27,6 +32,10 @@
  *   - ties in the top-K go to the lower logical page index; the selected list
  *     is returned in ascending page order, padded with -1;
  *   - only tokens t < seq_len count, in metadata and in attention;
+ *   - Block Top-K: a page's centroid is the mean of its valid keys, its
+ *     score for one query head is q . centroid, and with grouped-query
+ *     attention the page score is the maximum over the group's heads (the
+ *     same aggregation as for the bound);
  *   - an empty softmax (no token) gives output 0 and lse -inf.
  *
  * Element types: KV pools are read raw, as IEEE fp32 or as bfloat16 (the top
@@ -131,6 +140,63 @@ int orc_row_scores(const double *q_group, int G, const double *meta, int64_t n_p
         double best = -INFINITY;
         for (int h = 0; h < G; h++) {
             double s = orc_bound(q_group + (int64_t)h * d, mn, mx, d);
+            if (s > best) best = s;
+        }
+        scores[j] = best;
+    }
+    return rc;
+}
+
+/*
+ * [VX item 1] Block summaries of the listed physical pages: for every KV head
+ * g, c[i] = (1 / valid) * sum over the page's valid tokens t of K[t][i].
+ * cent is [n_pool][hkv][d]; pages not listed are left untouched.
+ * Returns 0, or -1 if a page id or a valid-token count is out of range.
+ */
+int orc_centroid(const void *k_pool, int kv_dtype, int64_t n_pool, int hkv, int page_size, int d,
+                 const int32_t *page_ids, const int32_t *valid_tokens, int64_t n_list, double *cent) {
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t e = 0; e < n_list; e++) {
+        int64_t p = page_ids[e];
+        int valid = valid_tokens[e];
+        if (p < 0 || p >= n_pool || valid < 1 || valid > page_size) {
+            bad = 1;
+            continue;
+        }
+        for (int g = 0; g < hkv; g++) {
+            double *c = cent + (p * hkv + g) * (int64_t)d;
+            for (int i = 0; i < d; i++) {
+                double sum = 0.0;
+                for (int t = 0; t < valid; t++)
+                    sum += load_elem(k_pool, kv_dtype, pool_index(p, hkv, g, page_size, t, d, i));
+                c[i] = sum / valid;
+            }
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * [VX item 1] Block Top-K scores of logical pages 0..n_b-1 of one sequence
+ * for KV head g: S(j) = max over the G query heads h of q_h . c_p,
+ * p = table_row[j].  Returns 0, or -1 on a bad page id (score -inf).
+ */
+int orc_centroid_scores(const double *q_group, int G, const double *cent, int64_t n_pool, int hkv, int g, int d,
+                        const int32_t *table_row, int n_b, double *scores) {
+    int rc = 0;
+    for (int j = 0; j < n_b; j++) {
+        int64_t p = table_row[j];
+        if (p < 0 || p >= n_pool) {
+            scores[j] = -INFINITY;
+            rc = -1;
+            continue;
+        }
+        const double *c = cent + (p * hkv + g) * (int64_t)d;
+        double best = -INFINITY;
+        for (int h = 0; h < G; h++) {
+            double s = 0.0;
+            for (int i = 0; i < d; i++) s += q_group[(int64_t)h * d + i] * c[i];
             if (s > best) best = s;
         }
         scores[j] = best;
@@ -254,7 +320,9 @@ int orc_attend_row(const double *q_group, int G, const void *k_pool, const void 
  * top_k <= 0 means every page (dense paged decode).
  *
  *   q            [B][Hq][d] double
- *   meta         [n_pool][hkv][2][d] double (ignored when dense)
+ *   meta         scorer 0: [n_pool][hkv][2][d] min/max rows; scorer 1: [n_pool][hkv][d]
+ *                centroids (double; ignored when dense)
+ *   scorer       0 = TinyServe bound [TS s2.2], 1 = Block Top-K centroid score [VX item 1]
  *   page_table   [B][max_pages] int32, seq_lens [B] int32
  *   selected_out [n_rows][max(top_k,1)] int32, n_sel_out [n_rows] (may be NULL when dense)
  *   scores_out   [n_rows][max_pages] double or NULL (-inf past n_b)
@@ -264,7 +332,7 @@ int orc_attend_row(const double *q_group, int G, const void *k_pool, const void 
  * number of threads used, or -1 if any row met a bad index.
  */
 int orc_step(const double *q, const void *k_pool, const void *v_pool, int kv_dtype, const double *meta,
-             const int32_t *page_table, const int32_t *seq_lens, int batch, int hq, int hkv, int d,
+             int scorer, const int32_t *page_table, const int32_t *seq_lens, int batch, int hq, int hkv, int d,
              int page_size, int max_pages, int64_t n_pool, int top_k, double sm_scale,
              const int32_t *rows, int n_rows, int32_t *selected_out, int32_t *n_sel_out,
              double *scores_out, double *out, double *lse) {
@@ -298,7 +366,10 @@ int orc_step(const double *q, const void *k_pool, const void *v_pool, int kv_dty
             const int32_t *list;
             int n_list;
             if (top_k > 0) {
-                if (orc_row_scores(q_group, G, meta, n_pool, hkv, g, d, table_row, n_b, scores) < 0) bad = 1;
+                int src = scorer == 1
+                              ? orc_centroid_scores(q_group, G, meta, n_pool, hkv, g, d, table_row, n_b, scores)
+                              : orc_row_scores(q_group, G, meta, n_pool, hkv, g, d, table_row, n_b, scores);
+                if (src < 0) bad = 1;
                 if (scores_out) {
                     for (int j = 0; j < max_pages; j++)
                         scores_out[(int64_t)e * max_pages + j] = j < n_b ? scores[j] : -INFINITY;

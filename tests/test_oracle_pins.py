@@ -358,3 +358,128 @@ def test_planted_pages_are_selected(oracle_lib):
         hits += len(set(pl) & set(res["selected"][e].tolist()))
         total += len(pl)
     assert total > 0 and hits == total
+
+
+# ------------------------------------------- Block Top-K (centroid) scorer --
+# Vortex sparse-attention digest, method overview item 1: the cache phase
+# keeps each block's mean key; the indexer scores q . centroid and keeps the
+# top-K blocks.
+
+@pytest.mark.parametrize("kv", [torch.float32, torch.bfloat16])
+def test_centroid_is_the_mean_of_the_valid_keys(oracle_lib, kv):
+    """Brute force: the per-dimension mean of the page's valid keys, taken by
+    numpy over the pool slice (fsum-accurate)."""
+    inp = _small(kv=kv)
+    ids, vt = oracle_lib.all_pages(inp)
+    cent = oracle_lib.centroids(inp["k_pool"], ids, vt)
+    kp = inp["k_pool"].double().numpy()
+    for p, v in zip(ids, vt):
+        want = np.array([[math.fsum(kp[p, g, :v, i]) / v for i in range(kp.shape[3])] for g in range(kp.shape[1])])
+        np.testing.assert_allclose(cent[p], want, rtol=1e-14, atol=1e-14)
+
+
+def test_centroid_special_cases(oracle_lib):
+    """A one-token page's centroid is the key; a page of identical keys has
+    that key as its centroid; NaN slots past the valid count never leak."""
+    inp = _small(seq_lens=(17, 8, 3))
+    kp = inp["k_pool"]
+    P = inp["spec"].page_size
+    p_one = int(inp["page_table"][0, 2])    # sequence 0, third page: 1 valid token
+    p_same = int(inp["page_table"][1, 0])   # sequence 1, first page: made constant
+    kp[p_same] = kp[p_same, :, :1, :].expand(-1, P, -1).clone()
+    ids = np.array([p_one, p_same], dtype=np.int32)
+    vt = np.array([1, P], dtype=np.int32)
+    cent = oracle_lib.centroids(kp, ids, vt)
+    np.testing.assert_array_equal(cent[p_one], kp[p_one, :, 0, :].double().numpy())
+    np.testing.assert_allclose(cent[p_same], kp[p_same, :, 0, :].double().numpy(), rtol=1e-15, atol=0)
+    p3 = int(inp["page_table"][2, 0])       # sequence 2: 3 valid tokens, NaN past them
+    assert torch.isnan(kp[p3, :, 3:]).all()
+    c3 = oracle_lib.centroids(kp, np.array([p3], dtype=np.int32), np.array([3], dtype=np.int32))
+    assert np.isfinite(c3[p3]).all()
+
+
+def test_centroid_score_is_the_mean_token_score(oracle_lib):
+    """Linearity: q . mean_t k_t equals the mean over the page's tokens of the
+    per-token logits q . k_t, computed token by token (brute force)."""
+    inp = _small(kv=torch.bfloat16, seq_lens=(45, 30), hq=6, hkv=2, d=16, P=8)
+    ids, vt = oracle_lib.all_pages(inp)
+    cent = oracle_lib.centroids(inp["k_pool"], ids, vt)
+    q = inp["q"].double().numpy()
+    kp = inp["k_pool"].double().numpy()
+    P, G = 8, 3
+    for b in range(2):
+        nb = int(inp["n_pages"][b])
+        L = int(inp["seq_lens"][b])
+        for g in range(2):
+            s = oracle_lib.centroid_row_scores(q[b, g * G:(g + 1) * G], cent, inp["page_table"][b], nb, g)
+            for j in range(nb):
+                p = int(inp["page_table"][b, j])
+                n = min(P, L - j * P)
+                per_head = [math.fsum(float(q[b, g * G + h] @ kp[p, g, t]) for t in range(n)) / n for h in range(G)]
+                assert abs(s[j] - max(per_head)) <= 1e-12 * (1 + abs(s[j]))
+
+
+def test_centroid_score_never_exceeds_the_bound(oracle_lib):
+    """Invariant tying the two scorers: a mean never exceeds a maximum, so for
+    every page and head q . centroid <= max_t q . k_t <= the TinyServe bound."""
+    inp = _small(kind="page_offset", kv=torch.bfloat16, seq_lens=(60, 33, 17), hq=4, hkv=2, d=16, P=8)
+    ids, vt = oracle_lib.all_pages(inp)
+    cent = oracle_lib.centroids(inp["k_pool"], ids, vt)
+    meta = oracle_lib.meta(inp["k_pool"], ids, vt)
+    q = inp["q"].double().numpy()
+    for b in range(3):
+        nb = int(inp["n_pages"][b])
+        for g in range(2):
+            qg = q[b, g * 2:(g + 1) * 2]
+            sc = oracle_lib.centroid_row_scores(qg, cent, inp["page_table"][b], nb, g)
+            sb = oracle_lib.row_scores(qg, meta, inp["page_table"][b], nb, g)
+            assert (sc <= sb + 1e-12 * (1 + np.abs(sb))).all()
+
+
+def test_centroid_shift_equivariance(oracle_lib):
+    """Adding a vector u to every key of the pool moves each centroid by u and
+    each head's score by q_h . u."""
+    inp = _small(kv=torch.float32, seq_lens=(24, 40), hq=2, hkv=1, d=8, P=8)
+    ids, vt = oracle_lib.all_pages(inp)
+    c0 = oracle_lib.centroids(inp["k_pool"], ids, vt)
+    u = torch.linspace(-1.0, 2.0, 8, dtype=torch.float64)
+    shifted = (inp["k_pool"].double() + u).to(torch.float32)
+    c1 = oracle_lib.centroids(shifted, ids, vt)
+    np.testing.assert_allclose(c1[ids] - c0[ids], np.broadcast_to(u.numpy(), c0[ids].shape), atol=1e-6)
+    q = inp["q"].double().numpy()
+    for b in range(2):
+        nb = int(inp["n_pages"][b])
+        for h in range(2):
+            s0 = oracle_lib.centroid_row_scores(q[b, h:h + 1], c0, inp["page_table"][b], nb, 0)
+            s1 = oracle_lib.centroid_row_scores(q[b, h:h + 1], c1, inp["page_table"][b], nb, 0)
+            np.testing.assert_allclose(s1 - s0, float(q[b, h] @ u.numpy()), atol=1e-5)
+
+
+def test_centroid_step_composes_and_finds_the_aligned_pages(oracle_lib):
+    """The batch driver with the centroid scorer equals its three steps one by
+    one; on the centroid workload (keys around 64 centroids, q near one) the
+    kept pages are exactly the best-aligned ones by brute force."""
+    spec = W.spec_for("long_context", batch=2, seq_len_range=(1500, 2500), max_pages=None, top_k=8)
+    inp = W.make_inputs(spec)
+    res = oracle_lib.step(inp, scorer="centroid")
+    cent = res["meta"]
+    q = inp["q"].double().numpy()
+    G, Hkv, P = spec.group, spec.num_kv_heads, spec.page_size
+    kp = inp["k_pool"].double().numpy()
+    for e, r in enumerate(res["rows"]):
+        b, g = divmod(int(r), Hkv)
+        nb = int(inp["n_pages"][b])
+        L = int(inp["seq_lens"][b])
+        s = oracle_lib.centroid_row_scores(q[b, g * G:(g + 1) * G], cent, inp["page_table"][b], nb, g)
+        np.testing.assert_array_equal(res["scores"][e, :nb], s)
+        sel, ns = oracle_lib.select(s, 8)
+        assert res["selected"][e].tolist() == sel.tolist() and res["n_sel"][e] == ns
+        # brute force: mean per-token logit per page, best of the group's heads
+        brute = []
+        for j in range(nb):
+            p = int(inp["page_table"][b, j])
+            n = min(P, L - j * P)
+            keys = kp[p, g, :n]
+            brute.append(max(float((keys @ q[b, g * G + h]).mean()) for h in range(G)))
+        order = sorted(range(nb), key=lambda j: (-brute[j], j))[:8]
+        assert sorted(order) == sel[:ns].tolist()
