@@ -49,7 +49,7 @@ def _es(dtype) -> int:
 
 
 def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray | None,
-               prefix_pages: int = 0) -> dict:
+               prefix_pages: int = 0, scorer: str = "bound") -> dict:
     """Algorithmic bytes of one step, per kernel.
 
     decode: K and V of every 16-token sub-tile holding a valid token of a
@@ -57,10 +57,11 @@ def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray
             selected list and one page-table entry per selected page; with
             a shared prefix of `prefix_pages` pages (cascade decode), the
             prefix pages once per KV head instead of once per sequence;
-    select: the metadata (2 d values) of every page of every row, q, one
-            page-table entry per page, the fp32 score written and read back,
-            the selected list written;
-    meta:   the valid key rows of each sequence's last page, its 2 d values written.
+    select: the metadata of every page of every row (2 d values in the KV
+            dtype for the bound scorer, d fp32 for the centroid scorer), q,
+            one page-table entry per page, the fp32 score written and read
+            back, the selected list written;
+    meta:   the valid key rows of each sequence's last page, its metadata written.
     """
     spec = inputs["spec"]
     B, Hq, Hkv, d, P = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
@@ -88,13 +89,14 @@ def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray
     top_k = spec.top_k
     sel_bytes = 0 if top_k is None else B * Hkv * top_k * 4 + B * Hkv * 4
     decode = kv + q_bytes + out_bytes + sel_bytes + n_pages_read * 4
+    meta_row = d * 4 if scorer == "centroid" else 2 * d * s
     if top_k is None:
         select = 0
     else:
         total_pages = int(nb.sum()) * Hkv
-        select = total_pages * (2 * d * s + 4 + 8) + q_bytes + sel_bytes
+        select = total_pages * (meta_row + 4 + 8) + q_bytes + sel_bytes
     last_valid = seq - (nb - 1) * P
-    meta = int(sum(int(v) * d * s + 2 * d * s for v in last_valid)) * Hkv
+    meta = int(sum(int(v) * d * s + meta_row for v in last_valid)) * Hkv
     return dict(decode=decode, select=select, meta=meta, total=decode + select + meta, kv=kv)
 
 
@@ -214,7 +216,8 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------- oracle --
-def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_target_s: float | None = None):
+def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_target_s: float | None = None,
+                  scorer: str = "bound"):
     """Times the CPU oracle (scores, top-K, attention) on a bounded sample of
     rows.  Returns (steps/s, cores, sample description, rows per step used)."""
     import oracle
@@ -224,12 +227,12 @@ def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_targ
     meta = None
     if spec.top_k is not None:
         ids, vt = oracle.all_pages(inputs)
-        meta = oracle.meta(inputs["k_pool"], ids, vt)
+        meta = (oracle.centroids if scorer == "centroid" else oracle.meta)(inputs["k_pool"], ids, vt)
     rng = np.random.default_rng(0)
     # calibrate on a small sample
     calib = rng.choice(n_rows, size=min(n_rows, max(threads, 8)), replace=False).astype(np.int32)
     t0 = time.perf_counter()
-    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv_cpu[0], threads=threads)
+    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv_cpu[0], threads=threads, scorer=scorer)
     dt = time.perf_counter() - t0
     rows_per_s = len(calib) / max(dt, 1e-9)
     cores = int(res["threads"])
@@ -239,7 +242,7 @@ def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_targ
     while t_total < budget_s or steps == 0:
         rows = rng.choice(n_rows, size=n, replace=False).astype(np.int32)
         t0 = time.perf_counter()
-        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv_cpu[steps % len(qv_cpu)], threads=threads)
+        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv_cpu[steps % len(qv_cpu)], threads=threads, scorer=scorer)
         t_total += time.perf_counter() - t0
         done_rows += n
         steps += 1
@@ -267,22 +270,22 @@ def run_reference(args):
     meta = None
     if spec.top_k is not None:
         ids, vt = oracle.all_pages(inputs)
-        meta = oracle.meta(inputs["k_pool"], ids, vt)
+        meta = (oracle.centroids if args.scorer == "centroid" else oracle.meta)(inputs["k_pool"], ids, vt)
     n_rows = spec.batch * spec.num_kv_heads
     rng = np.random.default_rng(0)
     calib = np.arange(min(n_rows, max(threads, 8)), dtype=np.int32)
     t0 = time.perf_counter()
-    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv[0], threads=threads)
+    res = oracle.step(inputs, rows=calib, meta_arr=meta, q=qv[0], threads=threads, scorer=args.scorer)
     rows_per_s = len(calib) / (time.perf_counter() - t0)
     n = int(min(n_rows, max(1, rows_per_s * per_step)))
     for i in range(args.warmup):
         oracle.step(inputs, rows=rng.choice(n_rows, size=n, replace=False).astype(np.int32), meta_arr=meta,
-                    q=qv[i % N_Q_VARIANTS], threads=threads)
+                    q=qv[i % N_Q_VARIANTS], threads=threads, scorer=args.scorer)
     t_total = 0.0
     for i in range(args.steps):
         rows = rng.choice(n_rows, size=n, replace=False).astype(np.int32)
         t0 = time.perf_counter()
-        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv[i % N_Q_VARIANTS], threads=threads)
+        oracle.step(inputs, rows=rows, meta_arr=meta, q=qv[i % N_Q_VARIANTS], threads=threads, scorer=args.scorer)
         t_total += time.perf_counter() - t0
     steps_per_s = (args.steps * n / n_rows) / t_total
     cores = int(res["threads"])
@@ -292,7 +295,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / steps_per_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec),
+        "config": workload_config(spec, args.scorer),
         "cpu_baseline": {"value": steps_per_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": steps_per_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -301,7 +304,7 @@ def run_reference(args):
     return 0
 
 
-def workload_config(spec: W.Spec) -> dict:
+def workload_config(spec: W.Spec, scorer: str = "bound") -> dict:
     desc = {
         "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
         "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
@@ -309,6 +312,8 @@ def workload_config(spec: W.Spec) -> dict:
         "shared_prefix": "shared-prefix dense decode (all pages), cascade: prefix once per KV head",
         "tiny": "tiny correctness batch",
     }.get(spec.name, spec.name)
+    if spec.top_k is not None and scorer == "centroid":
+        desc += " (Block Top-K centroid scorer)"
     return {"workload": desc, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
             "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page_size": spec.page_size,
             "seq_len": list(spec.seq_len_range) if spec.seq_len_range else
@@ -343,7 +348,7 @@ def run_gpu(args):
     inputs = W.make_inputs(spec)
     qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
     prefix = spec.prefix_pages if (spec.kind == "shared_prefix" and not args.no_cascade) else 0
-    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix)
+    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix, scorer=args.scorer)
     qv = qv_cpu.to(dev)
     ids, vt = W.all_pages(inputs)
     dec.build_meta(ids.to(dev), vt.to(dev))
@@ -357,7 +362,8 @@ def run_gpu(args):
         if spec.top_k is not None:
             dec.select(q=qv[v])
             torch.cuda.synchronize()
-            acc.append(step_bytes(inputs, dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy()))
+            acc.append(step_bytes(inputs, dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy(),
+                                  scorer=args.scorer))
         else:
             acc.append(step_bytes(inputs, None, None, prefix_pages=prefix))
             break
@@ -439,13 +445,13 @@ def run_gpu(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         sps, cores, sample, _ = oracle_sample(inputs, qv_cpu, budget_s=args.cpu_budget,
-                                              threads=os.cpu_count() or 1)
+                                              threads=os.cpu_count() or 1, scorer=args.scorer)
         cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": workload_config(spec),
+        "config": workload_config(spec, args.scorer),
         "effective_gbs": step_gbs,
         "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
         "bytes_per_step": nbytes,
@@ -483,6 +489,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--scorer", choices=["bound", "centroid"], default="bound",
+                    help="page score: TinyServe min/max bound (default) or Block Top-K centroid")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)

@@ -8,6 +8,11 @@
  *   qskv_sparse_paged_decode softmax(q K^T * scale) V over the selected pages,
  *                            split over warps and merged by log-sum-exp
  *
+ * with an alternative block score (the mean key of each page, "Block Top-K"):
+ *
+ *   qskv_kv_centroid_build     per-page mean key (fp32)
+ *   qskv_page_select_centroid  q . centroid of every page + top-K
+ *
  * and a dense decode for batches that share a prefix of pages:
  *
  *   qskv_cascade_paged_decode  the shared prefix once per KV head on the
@@ -27,6 +32,8 @@
  *   prefixes map to the same physical blocks).
  *   Quail AI-SQL engine article, "the inference engine as an execution
  *   engine": partial attention results combined by log-sum-exp rescaling.
+ *   Vortex digest, method overview item 1 (per-block mean keys scored by q,
+ *   "Block Top-K").
  *
  * Layouts (row-major, all on the device unless stated):
  *   k_pool, v_pool  [num_pool_pages][num_kv_heads][page_size][head_dim]  (kv dtype)
@@ -146,6 +153,37 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
                              const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
                              int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Block summaries for the Block Top-K scorer (Vortex sparse-attention digest,
+ * method overview item 1: the query-independent cache phase keeps each
+ * block's mean key, "centroids").  For each listed physical page p and every
+ * KV head g:
+ *   centroids[p][g][c] = (1 / valid_tokens[i]) * sum over t < valid_tokens[i]
+ *                        of k_pool[p][g][t][c]
+ * in fp32 (sums of fp32 values, whatever the kv dtype), layout
+ * [num_pool_pages][num_kv_heads][head_dim] fp32, 16-byte aligned.  Other
+ * pages are left untouched.  Same list semantics and device errors as
+ * qskv_kv_meta_build.
+ */
+qskv_status qskv_kv_centroid_build(const void *k_pool, qskv_dtype kv_dtype, const qskv_shape *shape,
+                                   const int32_t *page_ids, const int32_t *valid_tokens, int32_t n_pages,
+                                   float *centroids, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Page selection with the Block Top-K score (Vortex digest, method overview
+ * item 1: the query-dependent indexer phase scores blocks from q and their
+ * summaries and keeps the top-K).  For sequence b, KV head g and each logical
+ * page j < n_b, with p = page_table[b][j]:
+ *   S(j) = max over the group's query heads h of sum_c q[b][h][c] * centroids[p][g][c]
+ * computed in fp32; then exactly as qskv_page_select: the n = min(top_k, n_b)
+ * best pages (ties -> lower index), ascending, -1 padded; scores written to
+ * `scores` (or a workspace buffer); same workspace and device errors.
+ */
+qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const float *centroids,
+                                      const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
+                                      int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
+                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Sparse paged decode attention (TinyServe s2.3 stages 3-4; split-K with a

@@ -22,7 +22,8 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
           4: "QSKV_ERR_CUDA", 5: "QSKV_ERR_DEVICE_INDEX", 6: "QSKV_ERR_DEVICE_TIMEOUT"}
 
 # Every function the header declares, in declaration order.
-EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_sparse_paged_decode",
+EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_kv_centroid_build",
+           "qskv_page_select_centroid", "qskv_sparse_paged_decode",
            "qskv_sparse_paged_decode_noalloc", "qskv_cascade_workspace_size", "qskv_cascade_paged_decode",
            "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
 
@@ -66,6 +67,11 @@ def load(path: str = LIB_PATH):
     lib.qskv_page_select.restype = ctypes.c_int
     lib.qskv_page_select.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i32p, sp, i32, i32p, i32p, f32p, vp,
                                      sz, vp]
+    lib.qskv_kv_centroid_build.restype = ctypes.c_int
+    lib.qskv_kv_centroid_build.argtypes = [vp, ctypes.c_int, sp, i32p, i32p, i32, f32p, vp, sz, vp]
+    lib.qskv_page_select_centroid.restype = ctypes.c_int
+    lib.qskv_page_select_centroid.argtypes = [vp, ctypes.c_int, f32p, i32p, i32p, sp, i32, i32p, i32p, f32p, vp,
+                                              sz, vp]
     lib.qskv_sparse_paged_decode.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p, i32p, i32,
                                              ctypes.c_float, f32p, f32p, vp, sz, vp]
@@ -139,6 +145,30 @@ def page_select(q: torch.Tensor, meta: torch.Tensor, page_table: torch.Tensor, s
     _check(load().qskv_page_select(_ptr(q), _dtype(q), _ptr(meta), _dtype(meta), _ptr(page_table), _ptr(seq_lens),
                                    ctypes.byref(shape), int(top_k), _ptr(selected), _ptr(n_selected), _ptr(scores),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kv_centroid_build(k_pool: torch.Tensor, page_ids: torch.Tensor, valid_tokens: torch.Tensor,
+                      centroids: torch.Tensor, shape: Shape, workspace: torch.Tensor, stream=None):
+    """Per-(page, KV head) mean of the valid keys into fp32 ``centroids``
+    [Npool][Hkv][d] (the Block Top-K summary)."""
+    if centroids.dtype != torch.float32:
+        raise TypeError("centroids must be float32")
+    _check(load().qskv_kv_centroid_build(_ptr(k_pool), _dtype(k_pool), ctypes.byref(shape), _ptr(page_ids),
+                                         _ptr(valid_tokens), int(page_ids.numel()), _ptr(centroids),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
+
+
+def page_select_centroid(q: torch.Tensor, centroids: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                         top_k: int, selected: torch.Tensor, n_selected: torch.Tensor, shape: Shape,
+                         workspace: torch.Tensor, scores: Optional[torch.Tensor] = None, stream=None):
+    """Block Top-K selection: score q . centroid per page, keep the top_k."""
+    if centroids.dtype != torch.float32:
+        raise TypeError("centroids must be float32")
+    _check(load().qskv_page_select_centroid(_ptr(q), _dtype(q), _ptr(centroids), _ptr(page_table), _ptr(seq_lens),
+                                            ctypes.byref(shape), int(top_k), _ptr(selected), _ptr(n_selected),
+                                            _ptr(scores), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def sparse_paged_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor,

@@ -27,6 +27,8 @@
 // K-th key; a stable compaction in page order keeps every key above it and
 // the lowest-index keys equal to it.  The selected list comes out in
 // ascending page order.
+#include <type_traits>
+
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
 
@@ -410,7 +412,125 @@ __global__ void __launch_bounds__(kScoreThreads) score_simt_kernel(SelectArgs a,
     }
 }
 
+// ------------------------------------- Block Top-K scores (CUDA cores) --
+// Vortex sparse-attention digest, method overview item 1: a page's score is
+// q . centroid, the centroid being the page's mean key (fp32); with G query
+// heads per KV head the row score is the best head's.  HBM-bound like the
+// bound scorer (D fp32 per page, the same bytes as the bf16 [m | M] rows),
+// so it runs on the CUDA cores.  Lanes span the D dims of one page row
+// (coalesced), a warp takes 32 / G pages at a time so that the 32 (page,
+// head) partial dot products of a batch are reduced with one butterfly
+// reduce-scatter (31 shuffles; lane l ends with the total of (page l / G,
+// head l % G)), then a max over each group of G lanes.
+template <int D, bool QF32, int G>
+__global__ void __launch_bounds__(kScoreThreads) score_centroid_kernel(SelectArgs a, int score_all) {
+    constexpr int VEC = D / 32;  // dims per lane
+    constexpr int NPG = 32 / G;  // pages per batch
+    const RowInfo r = row_info(a);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *srow = a.scores + int64_t(r.row) * a.max_pages;
+    const int w_page0 = blockIdx.x * kScoreThreads + warp * 32;  // this warp's 32 pages
+    if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
+
+    // q of the group's heads, this lane's dims
+    float q[G][VEC];
+    const int64_t q0 = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * G) * D + lane * VEC;
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+#pragma unroll
+        for (int k = 0; k < VEC; k++) {
+            const int64_t qi = q0 + int64_t(h) * D + k;
+            q[h][k] = QF32 ? static_cast<const float *>(a.q)[qi]
+                           : __bfloat162float(static_cast<const __nv_bfloat16 *>(a.q)[qi]);
+        }
+    }
+    // page id of page w_page0 + lane (-1 past n_b, -2 when out of the pool)
+    int pid = -1;
+    if (w_page0 + lane < r.n_b) {
+        pid = a.page_table[int64_t(r.b) * a.max_pages + w_page0 + lane];
+        if (pid < 0 || pid >= a.num_pool_pages) {
+            raise_error(a.flags, kErrPageId);
+            pid = -2;
+        }
+    }
+    const float *cent = static_cast<const float *>(a.meta);
+    for (int p0 = 0; p0 < 32 && w_page0 + p0 < r.n_b; p0 += NPG) {
+        // loads of the batch's pages first
+        float c[NPG][VEC];
+#pragma unroll
+        for (int k = 0; k < NPG; k++) {
+            const int pk = __shfl_sync(0xffffffffu, pid, p0 + k);
+            const float *row = cent + (int64_t(pk < 0 ? 0 : pk) * a.num_kv_heads + r.g) * D + lane * VEC;
+            if (VEC == 4) {
+                const float4 x = pk >= 0 ? __ldg(reinterpret_cast<const float4 *>(row)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                c[k][0] = x.x;
+                c[k][VEC > 1 ? 1 : 0] = x.y;
+                c[k][VEC > 2 ? 2 : 0] = x.z;
+                c[k][VEC > 3 ? 3 : 0] = x.w;
+            } else {
+                const float2 x = pk >= 0 ? __ldg(reinterpret_cast<const float2 *>(row)) : make_float2(0.f, 0.f);
+                c[k][0] = x.x;
+                c[k][VEC > 1 ? 1 : 0] = x.y;
+            }
+        }
+        // 32 partial dots: slot k * G + h
+        float v[32];
+#pragma unroll
+        for (int sl = 0; sl < 32; sl++) {
+            const int k = sl / G, h = sl % G;
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; e++) acc = fmaf(q[h][e], c[k][e], acc);
+            v[sl] = acc;
+        }
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) {
+            const bool up = lane & s;
+#pragma unroll
+            for (int i = 0; i < s; i++) {
+                const float send = up ? v[i] : v[i + s];
+                const float keep = up ? v[i + s] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+            }
+        }
+        float best = v[0];  // lane l: (page p0 + l / G, head l % G)
+#pragma unroll
+        for (int off = 1; off < G; off <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
+        const int k = lane / G;
+        const int j = w_page0 + p0 + k;
+        const int pk = __shfl_sync(0xffffffffu, pid, (p0 + k) & 31);
+        if (lane % G == 0 && j < r.n_b) srow[j] = pk == -2 ? -INFINITY : best;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int head_dim, cudaStream_t stream,
+                                        int score_all) {
+    const int64_t rows = int64_t(a.batch) * a.num_kv_heads;
+    const dim3 grid(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
+    const dim3 block(kScoreThreads);
+    const bool qf = q_dtype == kDtypeF32;
+    cudaError_t e = cudaErrorInvalidValue;
+    auto go = [&](auto d_tag, auto q_tag) {
+        constexpr int D = decltype(d_tag)::value;
+        constexpr bool QF = decltype(q_tag)::value;
+        switch (a.group) {
+            case 1: e = launch_pdl(score_centroid_kernel<D, QF, 1>, grid, block, 0, stream, a, score_all); break;
+            case 2: e = launch_pdl(score_centroid_kernel<D, QF, 2>, grid, block, 0, stream, a, score_all); break;
+            case 4: e = launch_pdl(score_centroid_kernel<D, QF, 4>, grid, block, 0, stream, a, score_all); break;
+            case 8: e = launch_pdl(score_centroid_kernel<D, QF, 8>, grid, block, 0, stream, a, score_all); break;
+        }
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    if (head_dim == 128)
+        qf ? go(I128(), std::true_type()) : go(I128(), std::false_type());
+    else
+        qf ? go(I64(), std::true_type()) : go(I64(), std::false_type());
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_kernel, dim3(unsigned(rows)), dim3(kSelectThreads), 0, stream, a);
+}
 
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
                                int score_all) {

@@ -251,6 +251,78 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
                     "page_select launch");
 }
 
+qskv_status qskv_kv_centroid_build(const void *k_pool, qskv_dtype kv_dtype, const qskv_shape *shape,
+                                   const int32_t *page_ids, const int32_t *valid_tokens, int32_t n_pages,
+                                   float *centroids, void *workspace, size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (n_pages < 0) return fail(QSKV_ERR_INVALID_ARG, "n_pages must be >= 0 (got %d)", n_pages);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, 256));
+    if (n_pages == 0) return ok();
+    if (!k_pool || !page_ids || !valid_tokens || !centroids)
+        return fail(QSKV_ERR_INVALID_ARG, "k_pool, page_ids, valid_tokens and centroids must be non-NULL");
+    if (!aligned(k_pool, 16) || !aligned(centroids, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "k_pool and centroids must be 16-byte aligned");
+    if (!aligned(page_ids, 4) || !aligned(valid_tokens, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "page_ids and valid_tokens must be 4-byte aligned");
+    MetaArgs a;
+    a.k_pool = k_pool;
+    a.page_ids = page_ids;
+    a.valid_tokens = valid_tokens;
+    a.meta = centroids;
+    a.flags = static_cast<uint32_t *>(workspace);
+    a.n_list = n_pages;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.page_size = shape->page_size;
+    a.num_pool_pages = shape->num_pool_pages;
+    return launched(launch_centroid_build(a, kv_dtype, shape->head_dim, static_cast<cudaStream_t>(stream)),
+                    "kv_centroid_build launch");
+}
+
+qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const float *centroids,
+                                      const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
+                                      int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
+    if (!q || !centroids || !page_table || !seq_lens || !selected || !n_selected)
+        return fail(QSKV_ERR_INVALID_ARG,
+                    "q, centroids, page_table, seq_lens, selected and n_selected must be non-NULL");
+    if (!aligned(q, 16) || !aligned(centroids, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q and centroids must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(scores, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and score arrays must be 4-byte aligned");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    SelectArgs a;
+    a.q = q;
+    a.meta = centroids;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.scores = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = top_k;
+    return launched(launch_page_select_centroid(a, q_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
+                                                scores != nullptr),
+                    "page_select_centroid launch");
+}
+
 qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
                                      qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
                                      const qskv_shape *shape, const int32_t *selected, const int32_t *n_selected,

@@ -40,6 +40,10 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
                                  int extra_per_row = 0);
 
 cudaError_t launch_meta_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream);
+// Block Top-K: fp32 mean key per (page, KV head) into a.meta; scores q . centroid.
+cudaError_t launch_centroid_build(const MetaArgs &a, int kv_dtype, int head_dim, cudaStream_t stream);
+cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int head_dim, cudaStream_t stream,
+                                        int score_all);
 // score_all: compute scores even for rows where every page is kept.
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
                                int score_all);

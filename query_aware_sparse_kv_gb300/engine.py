@@ -25,10 +25,14 @@ class PagedDecoder:
     prefix_pages  logical pages [0, prefix_pages) every row shares (the same
                 physical pages): dense decodes then run as a cascade, the
                 prefix attended once per KV head for the whole batch
+    scorer      "bound" (TinyServe min/max metadata, the default) or
+                "centroid" (Block Top-K: fp32 mean key per page, q . centroid)
     """
 
     def __init__(self, q, k_pool, v_pool, page_table, seq_lens, top_k: Optional[int], sm_scale: float = 0.0,
-                 prefix_pages: int = 0):
+                 prefix_pages: int = 0, scorer: str = "bound"):
+        if scorer not in ("bound", "centroid"):
+            raise ValueError(f"unknown scorer {scorer!r}")
         dev = k_pool.device
         self.q, self.k_pool, self.v_pool = q, k_pool, v_pool
         self.page_table, self.seq_lens = page_table, seq_lens
@@ -38,7 +42,11 @@ class PagedDecoder:
         self.sm_scale = sm_scale
         self.shape = B.make_shape(batch, hq, hkv, d, P, page_table.shape[1], n_pool)
         self.prefix_pages = int(prefix_pages)
-        self.meta = torch.empty((n_pool, hkv, 2, d), dtype=k_pool.dtype, device=dev)
+        self.scorer = scorer
+        if scorer == "centroid":
+            self.meta = torch.empty((n_pool, hkv, d), dtype=torch.float32, device=dev)
+        else:
+            self.meta = torch.empty((n_pool, hkv, 2, d), dtype=k_pool.dtype, device=dev)
         ws = B.workspace_size(self.shape)
         if self.prefix_pages > 0:
             ws = max(ws, B.cascade_workspace_size(self.shape, self.prefix_pages))
@@ -51,12 +59,16 @@ class PagedDecoder:
 
     # -- cache phase ---------------------------------------------------------
     def build_meta(self, page_ids: torch.Tensor, valid_tokens: torch.Tensor, stream=None):
-        B.kv_meta_build(self.k_pool, page_ids, valid_tokens, self.meta, self.shape, self.workspace, stream)
+        if self.scorer == "centroid":
+            B.kv_centroid_build(self.k_pool, page_ids, valid_tokens, self.meta, self.shape, self.workspace, stream)
+        else:
+            B.kv_meta_build(self.k_pool, page_ids, valid_tokens, self.meta, self.shape, self.workspace, stream)
 
     # -- indexer phase -------------------------------------------------------
     def select(self, q=None, scores: Optional[torch.Tensor] = None, stream=None):
-        B.page_select(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k,
-                      self.selected, self.n_selected, self.shape, self.workspace, scores, stream)
+        fn = B.page_select_centroid if self.scorer == "centroid" else B.page_select
+        fn(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k, self.selected,
+           self.n_selected, self.shape, self.workspace, scores, stream)
 
     def decode(self, q=None, dense: bool = False, out=None, lse=None, stream=None):
         sel = None if (dense or self.top_k is None) else self.selected
@@ -102,10 +114,11 @@ class PagedDecoder:
             raise B.QskvError(st, B.last_error_message())
 
 
-def from_inputs(inputs: dict, device="cuda", top_k="spec", prefix_pages: int = 0) -> PagedDecoder:
+def from_inputs(inputs: dict, device="cuda", top_k="spec", prefix_pages: int = 0,
+                scorer: str = "bound") -> PagedDecoder:
     """A PagedDecoder over a workloads.make_inputs() batch copied to `device`."""
     if isinstance(top_k, str):
         top_k = inputs["top_k"]
     t = {k: inputs[k].to(device) for k in ("q", "k_pool", "v_pool", "page_table", "seq_lens")}
     return PagedDecoder(t["q"], t["k_pool"], t["v_pool"], t["page_table"], t["seq_lens"], top_k,
-                        prefix_pages=prefix_pages)
+                        prefix_pages=prefix_pages, scorer=scorer)

@@ -77,16 +77,56 @@ def assert_output_close(gpu_out, gpu_lse, oracle_out, oracle_lse, tol: float, wh
         assert e <= tol, f"{what} lse max-abs error {e} > {tol}"
 
 
+U32 = 2.0 ** -24  # unit roundoff of fp32
+
+
+def centroid_tolerance(k_pool: torch.Tensor, pages, valid) -> np.ndarray:
+    """Per-element bound of |fp32 centroid - exact mean| for the listed pages:
+    a sum of n fp32 values in any order is within (n - 1) u sum|k| of the
+    exact sum, and the division adds u |c|, so (sum/n) is within
+    n u max|k| of the mean.  Returns [Npool][Hkv][d] (0 for unlisted pages)."""
+    kp = k_pool.double().numpy()
+    tol = np.zeros((kp.shape[0], kp.shape[1], kp.shape[3]))
+    for p, v in zip(np.asarray(pages), np.asarray(valid)):
+        tol[p] = int(v) * U32 * np.abs(kp[p, :, :int(v), :]).max(axis=1)
+    return tol
+
+
+def assert_centroids_close(gpu_cent: torch.Tensor, oracle_cent: np.ndarray, tol: np.ndarray, pages) -> None:
+    g = gpu_cent.detach().cpu().double().numpy()
+    pages = np.asarray(pages, dtype=np.int64)
+    err = np.abs(g[pages] - oracle_cent[pages])
+    bound = tol[pages] + 1e-30
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert (err <= bound).all(), f"centroid error {err[worst]} > bound {bound[worst]} at {worst}"
+
+
+def centroid_score_tolerance(q_group: np.ndarray, cent: np.ndarray, cent_tol: np.ndarray, table_row, n_b: int,
+                             g: int) -> np.ndarray:
+    """Per-page bound of |fp32 score - exact score|: the centroid error
+    propagated (sum_i |q_i| tol_i) plus the d-term fp32 dot-product bound
+    (d u sum_i |q_i c_i|), the larger over the group's heads."""
+    d = q_group.shape[1]
+    out = np.zeros(n_b)
+    for j in range(n_b):
+        p = int(table_row[j])
+        c, t = cent[p, g], cent_tol[p, g]
+        out[j] = max(float(np.abs(qh) @ t + d * U32 * (np.abs(qh) @ np.abs(c))) for qh in q_group) * 1.01 + 1e-30
+    return out
+
+
 def n_pages_of(inputs: dict, b: int) -> int:
     P = inputs["spec"].page_size
     return (int(inputs["seq_lens"][b]) + P - 1) // P
 
 
 def check_rows(inputs: dict, dec, rows, oracle, oracle_meta=None, check_scores=None, dense: bool = False,
-               sm_scale=None):
+               sm_scale=None, scorer: str = "bound", cent_tol=None):
     """Compare the decoder's last results on `rows` (b * Hkv + g) with the
     oracle.  `dec` is a PagedDecoder whose select/decode already ran;
-    check_scores is the [B][Hkv][max_pages] GPU score tensor or None."""
+    check_scores is the [B][Hkv][max_pages] GPU score tensor or None.  With
+    scorer="centroid", oracle_meta holds the oracle's centroids and cent_tol
+    their error bounds (centroid_tolerance)."""
     spec = inputs["spec"]
     Hkv, G = spec.num_kv_heads, spec.group
     tol = out_tolerance(spec.kv_dtype)
@@ -102,9 +142,17 @@ def check_rows(inputs: dict, dec, rows, oracle, oracle_meta=None, check_scores=N
         if dense or spec.top_k is None:
             pages = list(range(n_b))
         else:
-            o_scores = oracle.row_scores(q[b, g * G:(g + 1) * G], oracle_meta, inputs["page_table"][b], n_b, g)
-            if check_scores is not None:
-                assert_scores_close(check_scores[b, g].cpu().numpy(), o_scores, n_b, what)
+            qg = q[b, g * G:(g + 1) * G]
+            if scorer == "centroid":
+                o_scores = oracle.centroid_row_scores(qg, oracle_meta, inputs["page_table"][b], n_b, g)
+                if check_scores is not None:
+                    stol = centroid_score_tolerance(qg, oracle_meta, cent_tol, inputs["page_table"][b], n_b, g)
+                    err = np.abs(check_scores[b, g].cpu().double().numpy()[:n_b] - o_scores)
+                    assert (err <= stol).all(), f"{what} centroid score error {err.max()} (bound {stol[np.argmax(err)]})"
+            else:
+                o_scores = oracle.row_scores(qg, oracle_meta, inputs["page_table"][b], n_b, g)
+                if check_scores is not None:
+                    assert_scores_close(check_scores[b, g].cpu().numpy(), o_scores, n_b, what)
             assert_selection_valid(sel[b, g], int(nsel[b, g]), o_scores, n_b, spec.top_k, what)
             pages = sel[b, g, :int(nsel[b, g])].tolist()
         o_out, o_lse = oracle.attend_row(inputs, b, g, pages, sm_scale=sm_scale)

@@ -118,6 +118,23 @@ def test_cascade_argument_checks(lib):
     assert lib.qskv_cascade_workspace_size(ctypes.byref(shape), 9) == 0
 
 
+def test_centroid_argument_checks(lib):
+    shape = qskv.make_shape(2, 8, 2, 128, 16, 8, 16)
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    # centroid build: negative count, NULL output, misaligned centroids, empty list is a no-op
+    assert lib.qskv_kv_centroid_build(p, 1, ctypes.byref(shape), p, p, -1, p, p, 4096, None) == 1
+    assert lib.qskv_kv_centroid_build(p, 1, ctypes.byref(shape), p, p, 2, None, p, 4096, None) == 1
+    assert lib.qskv_kv_centroid_build(p, 1, ctypes.byref(shape), p, p, 2, ctypes.c_void_p(base + 8), p, 4096,
+                                      None) == 1
+    assert lib.qskv_kv_centroid_build(p, 1, ctypes.byref(shape), p, p, 0, p, p, 4096, None) == 0
+    # selection: top_k < 1, NULL centroids, bad q dtype
+    assert lib.qskv_page_select_centroid(p, 1, p, p, p, ctypes.byref(shape), 0, p, p, None, p, 4096, None) == 1
+    assert lib.qskv_page_select_centroid(p, 1, None, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) == 1
+    assert lib.qskv_page_select_centroid(p, 9, p, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) == 2
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     saved = binding._lib
     binding._lib = None
