@@ -369,19 +369,38 @@ def run_gpu(args):
             break
     nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
 
-    def one_step(i, ev=None):
-        v = i % N_Q_VARIANTS
+    def select_part(v):
         dec.build_meta(last_ids, last_valid)
         if spec.top_k is not None:
             dec.select(q=qv[v])
-        if ev is not None:
-            ev[0].record(stream)
-        dec.decode(q=qv[v])
-        if ev is not None:
-            ev[1].record(stream)
 
+    def decode_part(v):
+        dec.decode(q=qv[v])
+
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()  # first use outside capture (kernel attributes, descriptors)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    # eager warm-up, then one CUDA graph per query variant for the whole step
+    # (the way a serving loop launches a decode step), and split graphs
+    # (selection part, decode part) for timing the decode call alone
     for i in range(args.warmup):
-        one_step(i)
+        select_part(i % N_Q_VARIANTS)
+        decode_part(i % N_Q_VARIANTS)
+    dec.check()
+    torch.cuda.synchronize()
+    step_graphs = [capture(lambda v=v: (select_part(v), decode_part(v))) for v in range(N_Q_VARIANTS)]
+    sel_graphs = [capture(lambda v=v: select_part(v)) for v in range(N_Q_VARIANTS)]
+    dec_graphs = [capture(lambda v=v: decode_part(v)) for v in range(N_Q_VARIANTS)]
+    for i in range(args.warmup):
+        step_graphs[i % N_Q_VARIANTS].replay()
     dec.check()
     torch.cuda.synchronize()
 
@@ -392,25 +411,47 @@ def run_gpu(args):
         pass
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        one_step(i, dec_ev[i])
+        step_graphs[i % N_Q_VARIANTS].replay()
     stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     barrier(world)
     elapsed_ms = start.elapsed_time(stop)
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
     clocks = None
     if sampler:
         time.sleep(0.25)
         sampler.stop()
         clocks = sampler.summary(wall0, wall1)
+
+    # decode call alone: events around the decode graph of each step
+    n_dec = min(args.steps, 1000)
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
+    for i in range(n_dec):
+        v = i % N_Q_VARIANTS
+        sel_graphs[v].replay()
+        dec_ev[i][0].record(stream)
+        dec_graphs[v].replay()
+        dec_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+
+    # the same step issued call by call from Python (launch-overhead diagnostic)
+    n_eager = min(args.steps, 300)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n_eager):
+        select_part(i % N_Q_VARIANTS)
+        decode_part(i % N_Q_VARIANTS)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n_eager
     dec.check()
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -462,6 +503,8 @@ def run_gpu(args):
                      "decode_ms": decode_ms, "bytes_per_launch": nbytes["decode"],
                      "traffic": ncu_traffic(args.workload)},
         "cpu_baseline": cpu,
+        "step_launch": "CUDA graph replay, one graph per query variant (meta refresh + selection + decode)",
+        "eager_ms_per_step": eager_ms,
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step replay",
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},

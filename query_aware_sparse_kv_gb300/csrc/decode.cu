@@ -1,4 +1,4 @@
-// Split-K sparse paged decode attention with a log-sum-exp merge.
+// Split-K sparse paged decode attention (the merge of split rows is in merge.cu).
 //
 // TinyServe query-aware page selection, s2.3 stages 3-4: only the selected
 // pages are loaded from HBM and attention runs while they stream in; s3.1:
@@ -94,98 +94,6 @@ __device__ __forceinline__ int unit_code_at(const DecodeArgs &a, int row, int sl
     const int s = slot + k;
     const int dr = s / a.slots_per_row;
     return unit_code(a, row + dr, s - dr * a.slots_per_row);
-}
-
-// Warps whose unit ranges intersect row `row` (none when there are no units).
-__device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t &w0, int64_t &w1) {
-    if (a.total_units == 0) {
-        w0 = 0;
-        w1 = -1;
-        return;
-    }
-    const int64_t first = int64_t(row) * a.slots_per_row;
-    const int64_t last = min(first + a.slots_per_row, a.total_units) - 1;
-    w0 = first / a.units_per_warp;
-    w1 = last / a.units_per_warp;
-}
-
-// A warp that covers a whole row writes the final output itself, unless
-// another kernel contributes pieces to the row.
-__device__ __forceinline__ bool row_is_final(const DecodeArgs &a, int64_t w0, int64_t w1) {
-    return w0 == w1 && a.extra_pieces == 0;
-}
-
-// LSE merge of the split partials (one CTA per row).  Row `row` was split
-// over warps w0..w1; warp w left a normalised partial o_w and its log2-domain
-// log-sum-exp in slot row + w; another kernel may have left extra_pieces more
-// in slots extra_slot0 + row * extra_pieces + e (the shared-prefix part of a
-// cascade decode).  out = sum_w 2^(lse_w - m) o_w / sum_w 2^(lse_w - m),
-// lse = m + log2 sum_w 2^(lse_w - m), taken in one pass with a running
-// maximum m; each thread owns one float4 of the row's G x D output and keeps
-// eight slots' loads in flight.  Rows a single warp covered alone were
-// finished by that warp.
-template <int D>
-__global__ void __launch_bounds__(128) merge_partials_kernel(DecodeArgs a) {
-    pdl_trigger();
-    pdl_wait();
-    const int row = blockIdx.x;
-    int64_t w0, w1;
-    row_warps(a, row, w0, w1);
-    if (row_is_final(a, w0, w1)) return;
-    constexpr int V4 = D / 4;
-    constexpr int SC = 8;
-    const int G = a.group;
-    const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
-    const int nd = int(w1 - w0 + 1);  // pieces from decode warps: slots row + w0 ..
-    const int ne = a.extra_pieces;    // pieces from another kernel: slots extra_slot0 + row * ne ..
-    const int64_t slot_d = row + w0, slot_e = a.extra_slot0 + int64_t(row) * ne;
-    const float4 *o_all = reinterpret_cast<const float4 *>(a.part_o);
-    const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
-    for (int it = threadIdx.x; it < G * V4; it += blockDim.x) {
-        const int h = it / V4, c4 = it % V4;
-        float mx = -INFINITY, den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        // folds n consecutive slots into (mx, den, acc)
-        auto fold = [&](const float *lse_p, const float4 *o_p, int n) {
-            for (int s0 = 0; s0 < n; s0 += SC) {
-                float l[SC];
-                float4 v[SC];
-#pragma unroll
-                for (int j = 0; j < SC; j++) {
-                    const bool ok = s0 + j < n;
-                    l[j] = ok ? __ldcg(lse_p + (s0 + j) * G) : -INFINITY;
-                    v[j] = ok && l[j] != -INFINITY ? __ldcg(o_p + (s0 + j) * G * V4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                float m = mx;
-#pragma unroll
-                for (int j = 0; j < SC; j++) m = fmaxf(m, l[j]);
-                if (m == -INFINITY) continue;
-                const float sc = exp2f(mx - m);
-                den *= sc;
-                acc.x *= sc;
-                acc.y *= sc;
-                acc.z *= sc;
-                acc.w *= sc;
-#pragma unroll
-                for (int j = 0; j < SC; j++) {
-                    if (l[j] == -INFINITY) continue;  // an empty piece: its o was never written
-                    const float w = exp2f(l[j] - m);
-                    den += w;
-                    acc.x = fmaf(w, v[j].x, acc.x);
-                    acc.y = fmaf(w, v[j].y, acc.y);
-                    acc.z = fmaf(w, v[j].z, acc.z);
-                    acc.w = fmaf(w, v[j].w, acc.w);
-                }
-                mx = m;
-            }
-        };
-        fold(a.part_lse + slot_d * G + h, o_all + slot_d * G * V4 + it, nd);
-        if (ne > 0) fold(a.part_lse + slot_e * G + h, o_all + slot_e * G * V4 + it, ne);
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (c4 == 0 && a.lse) a.lse[qh0 + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
-    }
 }
 
 // ------------------------------------------------- bf16 KV, tensor cores --
@@ -731,11 +639,6 @@ size_t decode_smem_bytes(int head_dim, int stages) {
     return stage * size_t(stages) * size_t(decode_warps_per_cta(head_dim)) + 1024;
 }
 
-static cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t stream) {
-    const dim3 g(unsigned(int64_t(a.batch) * a.num_kv_heads)), b(128);
-    return head_dim == 128 ? launch_pdl(merge_partials_kernel<128>, g, b, 0, stream, a)
-                           : launch_pdl(merge_partials_kernel<64>, g, b, 0, stream, a);
-}
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
                           int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream,

@@ -369,6 +369,25 @@ constexpr int kPrefixRowThreads = 2;  // softmax threads per query row (each own
 constexpr int kPrefixThreads = 128 * kPrefixRowThreads + 96;  // softmax warps, MMA warp, K and V TMA warps
 constexpr int kMaxPrefixSplits = 64;
 
+// Warps whose unit ranges intersect row `row` (none when there are no units).
+__device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t &w0, int64_t &w1) {
+    if (a.total_units == 0) {
+        w0 = 0;
+        w1 = -1;
+        return;
+    }
+    const int64_t first = int64_t(row) * a.slots_per_row;
+    const int64_t last = min(first + a.slots_per_row, a.total_units) - 1;
+    w0 = first / a.units_per_warp;
+    w1 = last / a.units_per_warp;
+}
+
+// A warp that covers a whole row writes the final output itself, unless
+// another kernel contributes pieces to the row.
+__device__ __forceinline__ bool row_is_final(const DecodeArgs &a, int64_t w0, int64_t w1) {
+    return w0 == w1 && a.extra_pieces == 0;
+}
+
 constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
 constexpr int kSelectThreads = 256;   // ranking CTA: one row
 constexpr int kSelectKeyCap = 4096;   // keys held in shared memory by the select stage

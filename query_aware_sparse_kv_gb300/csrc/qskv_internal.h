@@ -53,6 +53,9 @@ cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype,
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
                           int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream,
                           const PrefixArgs *prefix = nullptr);
+// LSE merge of the decode rows split over several warps (and of another
+// kernel's extra pieces); launched after the decode grid.
+cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t stream);
 // Shared-prefix attention of a cascade decode: 128-row query tiles per KV
 // head, and the key splits per (tile, head) chosen for a device with
 // `num_sms` SMs (0 when the prefix is empty).
