@@ -13,7 +13,9 @@ Every function states the passage it follows:
   block tables and shared prefixes;
   Quail AI-SQL engine article -- partial attention merged by log-sum-exp;
   Vortex sparse-attention digest, method overview item 1 -- per-block mean
-  keys ("centroids") from the cache phase, Block Top-K scoring q . centroid.
+  keys ("centroids") from the cache phase, Block Top-K scoring q . centroid;
+  item 3 -- a lossy radix Top-K with early exit and random sampling from the
+  threshold bin (its random numbers from SplitMix64, Steele, Lea and Flood 2014).
 """
 
 from __future__ import annotations
@@ -65,6 +67,11 @@ def _load():
         lib.orc_centroid_scores.restype = ctypes.c_int
         lib.orc_centroid_scores.argtypes = [_f64p, ctypes.c_int, _f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, _i32p, ctypes.c_int, _f64p]
+        lib.orc_splitmix64.restype = ctypes.c_uint64
+        lib.orc_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.orc_select_approx.restype = ctypes.c_int
+        lib.orc_select_approx.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_uint64, ctypes.c_int64, _i32p]
         lib.orc_select.restype = ctypes.c_int
         lib.orc_select.argtypes = [_f64p, ctypes.c_int, ctypes.c_int, _i32p]
         lib.orc_attend_row.restype = ctypes.c_int
@@ -183,6 +190,28 @@ def select(scores, top_k: int) -> tuple[np.ndarray, int]:
     s = _f64(scores)
     sel = np.empty(max(top_k, 1), dtype=np.int32)
     n = _load().orc_select(_p(s, _f64p), len(s), top_k, _p(sel, _i32p))
+    return sel[:top_k], n
+
+
+def splitmix64(seed: int, i: int) -> int:
+    """Output i of SplitMix64 started at `seed` (Steele, Lea and Flood 2014)."""
+    return int(_load().orc_splitmix64(seed & (2 ** 64 - 1), i & (2 ** 64 - 1)))
+
+
+def need_max(top_k: int, epsilon: float) -> int:
+    """Early-exit threshold of the approximate top-K: floor(epsilon * K)."""
+    return int(math.floor(epsilon * top_k))
+
+
+def select_approx(scores_f32, top_k: int, epsilon: float, seed: int, row: int) -> tuple[np.ndarray, int]:
+    """Vortex item 3: lossy radix top-K over fp32 scores -- exact radix passes
+    until at most floor(epsilon * K) keys are undecided, then those drawn by
+    systematic random sampling from the threshold bin.  epsilon = 0 is the
+    exact rule.  Returns (ascending indices, -1 padded to top_k; count)."""
+    s = np.ascontiguousarray(scores_f32, dtype=np.float32)
+    sel = np.empty(max(top_k, 1), dtype=np.int32)
+    n = _load().orc_select_approx(s.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), len(s), top_k,
+                                  need_max(top_k, epsilon), seed & (2 ** 64 - 1), row, _p(sel, _i32p))
     return sel[:top_k], n
 
 

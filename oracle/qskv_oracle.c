@@ -19,6 +19,12 @@
  *   [QU]  Quail AI-SQL engine article, section "the inference engine as an
  *         execution engine" (partial attention results combined by
  *         log-sum-exp rescaling, as in flash decoding).
+ *   [VXR] Vortex digest, method overview item 3: a lossy radix Top-K that
+ *         stops once enough high-confidence candidates are collected and
+ *         draws the rest at random from the threshold bin (recall@k > 0.97).
+ *   [SM]  SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
+ *         number generators", OOPSLA 2014): state_i = seed + i * gamma,
+ *         output_i = mix(state_i), used as a counter-based generator.
  *   [VX]  Vortex sparse-attention digest, method overview item 1: a
  *         query-independent cache phase computes per-block summaries such as
  *         the block's mean key ("centroids"); the query-dependent indexer
@@ -312,6 +318,104 @@ int orc_attend_row(const double *q_group, int G, const void *k_pool, const void 
     free(logit);
     free(tok_base);
     return rc < 0 ? -1 : n_tok;
+}
+
+/* [SM] Output i (i >= 1) of SplitMix64 started at `seed`. */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + i * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+/* fp32 score -> unsigned key with the same order (-0 and +0 share a key). */
+static uint32_t key_of(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/*
+ * [VXR] Approximate top-K of one row of fp32 scores (the reading taken for
+ * the digest's lossy radix Top-K):
+ *   1. scores become order-preserving 32-bit keys;
+ *   2. MSB-first radix passes over 8-bit digits, starting at the highest bit
+ *      where the row's keys differ: each pass counts the keys of the current
+ *      bucket per digit and moves into the digit bucket that holds the
+ *      `need`-th largest key; keys in higher digit buckets are certain to be
+ *      in the top-K and leave `need`;
+ *   3. early exit: before a pass, if need <= need_max (= floor(eps * K)),
+ *      stop; also stop when the bucket is taken whole or fully resolved;
+ *   4. the keys above the final bucket are all kept; `need` keys of the
+ *      bucket (m keys, ranked t = 0..m-1 in page order) are kept: exactly
+ *      those t with floor(((t + 1) need + o) / m) - floor((t need + o) / m) = 1,
+ *      o = splitmix64(seed, row + 1) mod m (systematic sampling with a random
+ *      start: every key of the bucket is kept with probability need / m).
+ *      need_max = 0 gives the exact rule instead: the first `need` in page
+ *      order (ties -> lower index).
+ * selected gets the kept indices ascending, -1 padded to top_k; returns the
+ * count min(top_k, n).
+ */
+int orc_select_approx(const float *scores, int n, int top_k, int need_max, uint64_t seed, int64_t row,
+                      int32_t *selected) {
+    if (top_k >= n) {
+        for (int i = 0; i < top_k; i++) selected[i] = i < n ? i : -1;
+        return n;
+    }
+    uint32_t *key = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = 0; i < n; i++) {
+        key[i] = key_of(scores[i]);
+        if (key[i] < kmin) kmin = key[i];
+        if (key[i] > kmax) kmax = key[i];
+    }
+    uint32_t diff = kmin ^ kmax;
+    int hi = 0;
+    while (hi < 32 && (diff >> hi) != 0u) hi++; /* bits >= hi are common to all keys */
+    uint64_t prefix = hi >= 32 ? 0u : ((uint64_t)kmax >> hi) << hi;
+    int need = top_k, lo = hi;
+    while (hi > 0) {
+        if (need_max > 0 && need <= need_max) break;
+        lo = hi > 8 ? hi - 8 : 0;
+        uint64_t count[256] = {0};
+        for (int i = 0; i < n; i++)
+            if (((uint64_t)key[i] >> hi) == (prefix >> hi)) count[(key[i] >> lo) & ((1u << (hi - lo)) - 1u)]++;
+        uint64_t above = 0;
+        int bin = -1;
+        for (int d = (1 << (hi - lo)) - 1; d >= 0; d--) {
+            if (above + count[d] >= (uint64_t)need) {
+                bin = d;
+                break;
+            }
+            above += count[d];
+        }
+        prefix |= (uint64_t)bin << lo;
+        need -= (int)above;
+        if ((int)count[bin] == need) break;
+        hi = lo;
+    }
+    uint64_t thr = prefix >> lo;
+    int64_t m = 0;
+    for (int i = 0; i < n; i++) m += ((uint64_t)key[i] >> lo) == thr;
+    uint64_t o = need_max > 0 ? orc_splitmix64(seed, (uint64_t)row + 1u) % (uint64_t)m : 0;
+    int out = 0;
+    int64_t t = 0;
+    for (int i = 0; i < n; i++) {
+        uint64_t k = (uint64_t)key[i] >> lo;
+        if (k > thr) {
+            selected[out++] = i;
+        } else if (k == thr) {
+            int take = need_max > 0 ? (int)(((uint64_t)(t + 1) * need + o) / (uint64_t)m -
+                                             ((uint64_t)t * need + o) / (uint64_t)m)
+                                    : t < need;
+            if (take) selected[out++] = i;
+            t++;
+        }
+    }
+    for (int i = out; i < top_k; i++) selected[i] = -1;
+    free(key);
+    return out;
 }
 
 /*
