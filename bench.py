@@ -295,7 +295,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / steps_per_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, args.scorer),
+        "config": workload_config(spec, args.scorer, args.approx_eps),
         "cpu_baseline": {"value": steps_per_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": steps_per_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -304,7 +304,7 @@ def run_reference(args):
     return 0
 
 
-def workload_config(spec: W.Spec, scorer: str = "bound") -> dict:
+def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None) -> dict:
     desc = {
         "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
         "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
@@ -314,6 +314,8 @@ def workload_config(spec: W.Spec, scorer: str = "bound") -> dict:
     }.get(spec.name, spec.name)
     if spec.top_k is not None and scorer == "centroid":
         desc += " (Block Top-K centroid scorer)"
+    if spec.top_k is not None and approx_eps is not None:
+        desc += f" (lossy top-K, eps {approx_eps:g})"
     return {"workload": desc, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
             "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page_size": spec.page_size,
             "seq_len": list(spec.seq_len_range) if spec.seq_len_range else
@@ -348,7 +350,8 @@ def run_gpu(args):
     inputs = W.make_inputs(spec)
     qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
     prefix = spec.prefix_pages if (spec.kind == "shared_prefix" and not args.no_cascade) else 0
-    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix, scorer=args.scorer)
+    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix, scorer=args.scorer,
+                           approx_epsilon=args.approx_eps, approx_seed=args.seed)
     qv = qv_cpu.to(dev)
     ids, vt = W.all_pages(inputs)
     dec.build_meta(ids.to(dev), vt.to(dev))
@@ -492,7 +495,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": workload_config(spec, args.scorer),
+        "config": workload_config(spec, args.scorer, args.approx_eps),
         "effective_gbs": step_gbs,
         "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
         "bytes_per_step": nbytes,
@@ -534,6 +537,9 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
     ap.add_argument("--scorer", choices=["bound", "centroid"], default="bound",
                     help="page score: TinyServe min/max bound (default) or Block Top-K centroid")
+    ap.add_argument("--approx-eps", type=float, default=None,
+                    help="lossy top-K: stop once floor(eps * K) pages are undecided and sample them")
+    ap.add_argument("--seed", type=int, default=0, help="seed of the lossy top-K's sampling")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)

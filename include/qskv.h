@@ -96,6 +96,10 @@ typedef enum {
 
 typedef enum { QSKV_F32 = 0, QSKV_BF16 = 1 } qskv_dtype;
 
+/* Page score of the selection calls: the TinyServe bound over min/max
+ * metadata, or the Block Top-K dot product with the mean key. */
+typedef enum { QSKV_SCORE_BOUND = 0, QSKV_SCORE_CENTROID = 1 } qskv_scorer;
+
 typedef struct {
     int32_t batch;          /* B: sequences */
     int32_t num_q_heads;    /* Hq */
@@ -184,6 +188,30 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
                                       const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
                                       int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Page selection with a lossy top-K (Vortex digest, method overview item 3:
+ * a radix Top-K that stops once enough high-confidence candidates are
+ * collected and draws the rest at random from the threshold bin; the digest
+ * reports recall@k > 0.97 at 1.3-1.6x the exact kernel's speed).
+ * Scores as qskv_page_select (scorer QSKV_SCORE_BOUND: meta = [m | M] rows in
+ * meta_dtype) or qskv_page_select_centroid (QSKV_SCORE_CENTROID: meta = fp32
+ * centroids, meta_dtype QSKV_F32).  Ranking: the exact MSB-first radix passes
+ * over 8-bit digits of the order-preserving score keys run until at most
+ * floor(epsilon * top_k) keys are undecided; every key above the threshold
+ * digit bucket is kept, and the `need` still missing are drawn from that
+ * bucket's m keys (ranked t = 0..m-1 in page order) by systematic sampling:
+ * key t is kept iff floor(((t+1) need + o) / m) - floor((t need + o) / m) = 1,
+ * with o = SplitMix64 output (row + 1) from `seed` (Steele, Lea and Flood
+ * 2014), mod m.  Hence recall@top_k >= 1 - epsilon against the exact top-K
+ * of the same fp32 scores, exactly min(top_k, n_b) pages, ascending.
+ * epsilon in [0, 1); 0 gives exactly qskv_page_select's result.
+ */
+qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtype q_dtype, const void *meta,
+                                    qskv_dtype meta_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                    const qskv_shape *shape, int32_t top_k, float epsilon, uint64_t seed,
+                                    int32_t *selected, int32_t *n_selected, float *scores, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /*
  * Sparse paged decode attention (TinyServe s2.3 stages 3-4; split-K with a

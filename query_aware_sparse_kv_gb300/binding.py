@@ -23,7 +23,7 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
 
 # Every function the header declares, in declaration order.
 EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_kv_centroid_build",
-           "qskv_page_select_centroid", "qskv_sparse_paged_decode",
+           "qskv_page_select_centroid", "qskv_page_select_approx", "qskv_sparse_paged_decode",
            "qskv_sparse_paged_decode_noalloc", "qskv_cascade_workspace_size", "qskv_cascade_paged_decode",
            "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
 
@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH):
     lib.qskv_page_select_centroid.restype = ctypes.c_int
     lib.qskv_page_select_centroid.argtypes = [vp, ctypes.c_int, f32p, i32p, i32p, sp, i32, i32p, i32p, f32p, vp,
                                               sz, vp]
+    lib.qskv_page_select_approx.restype = ctypes.c_int
+    lib.qskv_page_select_approx.argtypes = [ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int, i32p, i32p, sp, i32,
+                                            ctypes.c_float, ctypes.c_uint64, i32p, i32p, f32p, vp, sz, vp]
     lib.qskv_sparse_paged_decode.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p, i32p, i32,
                                              ctypes.c_float, f32p, f32p, vp, sz, vp]
@@ -169,6 +172,23 @@ def page_select_centroid(q: torch.Tensor, centroids: torch.Tensor, page_table: t
                                             ctypes.byref(shape), int(top_k), _ptr(selected), _ptr(n_selected),
                                             _ptr(scores), _ptr(workspace),
                                             workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+SCORERS = {"bound": 0, "centroid": 1}
+
+
+def page_select_approx(q: torch.Tensor, meta: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                       top_k: int, selected: torch.Tensor, n_selected: torch.Tensor, shape: Shape,
+                       workspace: torch.Tensor, epsilon: float, seed: int, scorer: str = "bound",
+                       scores: Optional[torch.Tensor] = None, stream=None):
+    """Selection with the lossy top-K: radix passes until at most
+    floor(epsilon * top_k) pages are undecided, the rest sampled from the
+    threshold bucket (random start from SplitMix64(seed))."""
+    _check(load().qskv_page_select_approx(SCORERS[scorer], _ptr(q), _dtype(q), _ptr(meta), _dtype(meta),
+                                          _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(top_k),
+                                          float(epsilon), int(seed) & (2 ** 64 - 1), _ptr(selected),
+                                          _ptr(n_selected), _ptr(scores), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def sparse_paged_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor,

@@ -67,8 +67,9 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
 }
 
 // --------------------------------------------------------------- select --
+// Exclusive block scans of x and y; total_y gets the sum of y over the block.
 template <int NT>
-__device__ __forceinline__ void block_exclusive_scan2(int &x, int &y, int *s_tmp /* 2*NT/32 */) {
+__device__ __forceinline__ void block_exclusive_scan2(int &x, int &y, int &total_y, int *s_tmp /* 2*NT/32 */) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int ix = x, iy = y;
 #pragma unroll
@@ -85,14 +86,28 @@ __device__ __forceinline__ void block_exclusive_scan2(int &x, int &y, int *s_tmp
         s_tmp[NT / 32 + warp] = iy;
     }
     __syncthreads();
-    int ox = 0, oy = 0;
-    for (int w = 0; w < warp; w++) {
-        ox += s_tmp[w];
-        oy += s_tmp[NT / 32 + w];
+    int ox = 0, oy = 0, ty = 0;
+    for (int w = 0; w < NT / 32; w++) {
+        if (w < warp) {
+            ox += s_tmp[w];
+            oy += s_tmp[NT / 32 + w];
+        }
+        ty += s_tmp[NT / 32 + w];
     }
     x = ox + ix - x;
     y = oy + iy - y;
+    total_y = ty;
     __syncthreads();
+}
+
+// Output i (i >= 1) of SplitMix64 started at `seed` (Steele, Lea and Flood,
+// "Fast splittable pseudorandom number generators", 2014), used as a
+// counter-based generator: the random start of a row's sample.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + i * 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
 }
 
 // Ranks one row's scores (all threads of the CTA take part).
@@ -166,6 +181,8 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
     int need = K;  // keys still to take among those matching `prefix` above `hi`
     int lo = hi;
     while (hi > 0) {
+        // lossy early exit: few enough keys are still undecided
+        if (a.need_max > 0 && need <= a.need_max) break;
         lo = hi > 8 ? hi - 8 : 0;
         const uint32_t mask = (1u << (hi - lo)) - 1u;
         s_hist[tid] = 0u;  // NT == 256 bins
@@ -209,8 +226,13 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
         hi = lo;
     }
 
-    // Stable compaction in page order: keys above the threshold, then the
-    // first `need` keys equal to it.
+    // Stable compaction in page order: every key above the threshold bucket,
+    // and `need` of the bucket's m keys.  Exact rule: the first `need` in
+    // page order.  After a lossy early exit: bucket key t (0-based, page
+    // order) is kept iff c(t + 1) - c(t) = 1 with c(t) = (t need + o) / m
+    // (integer division; o = a SplitMix64 draw mod m): systematic sampling
+    // with a random start, every bucket key kept with probability need / m.
+    // Either way c(t) keys of the bucket precede bucket key t in the output.
     const uint32_t thr = shr32(prefix, lo);
     const int per = (n_b + NT - 1) / NT;
     const int i0 = min(tid * per, n_b), i1 = min(i0 + per, n_b);
@@ -220,17 +242,42 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
         cg += k > thr;
         ce += k == thr;
     }
-    int gb = cg, eb = ce;
-    block_exclusive_scan2<NT>(gb, eb, s_tmp);
-    for (int i = i0; i < i1; i++) {
-        const uint32_t k = shr32(key_at(i), lo);
-        if (k > thr) {
-            const int pos = gb + min(eb, need);
-            if (pos < K) sel[pos] = i;
-            gb++;
-        } else if (k == thr) {
-            if (eb < need && gb + eb < K) sel[gb + eb] = i;
-            eb++;
+    int gb = cg, eb = ce, m = 0;
+    block_exclusive_scan2<NT>(gb, eb, m, s_tmp);
+    const bool sampled = a.need_max > 0 && need < m;
+    if (!sampled) {
+        for (int i = i0; i < i1; i++) {
+            const uint32_t k = shr32(key_at(i), lo);
+            if (k > thr) {
+                const int pos = gb + min(eb, need);
+                if (pos < K) sel[pos] = i;
+                gb++;
+            } else if (k == thr) {
+                if (eb < need && gb + eb < K) sel[gb + eb] = i;
+                eb++;
+            }
+        }
+    } else {
+        // c(t) and the remainder of (t need + o) by m, stepped per bucket key
+        // (t need + o < m (need + 1) < 2^32 for rows held in shared memory)
+        const uint64_t o = splitmix64(a.seed, uint64_t(row) + 1u) % uint64_t(m);
+        const uint64_t x = uint64_t(eb) * uint64_t(need) + o;
+        int c = int(x / uint64_t(m));
+        int rem = int(x - uint64_t(c) * uint64_t(m));
+        for (int i = i0; i < i1; i++) {
+            const uint32_t k = shr32(key_at(i), lo);
+            if (k > thr) {
+                const int pos = gb + c;
+                if (pos < K) sel[pos] = i;
+                gb++;
+            } else if (k == thr) {
+                rem += need;
+                if (rem >= m) {  // c(t + 1) = c(t) + 1: this key is kept
+                    rem -= m;
+                    if (gb + c < K) sel[gb + c] = i;
+                    c++;
+                }
+            }
         }
     }
     if (tid == 0) a.n_selected[row] = K;

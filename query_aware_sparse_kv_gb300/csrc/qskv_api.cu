@@ -246,6 +246,8 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     a.max_pages = shape->max_pages;
     a.num_pool_pages = shape->num_pool_pages;
     a.top_k = top_k;
+    a.need_max = 0;
+    a.seed = 0;
     return launched(launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                        scores != nullptr),
                     "page_select launch");
@@ -318,9 +320,64 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
     a.max_pages = shape->max_pages;
     a.num_pool_pages = shape->num_pool_pages;
     a.top_k = top_k;
+    a.need_max = 0;
+    a.seed = 0;
     return launched(launch_page_select_centroid(a, q_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                                 scores != nullptr),
                     "page_select_centroid launch");
+}
+
+qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtype q_dtype, const void *meta,
+                                    qskv_dtype meta_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                    const qskv_shape *shape, int32_t top_k, float epsilon, uint64_t seed,
+                                    int32_t *selected, int32_t *n_selected, float *scores, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(meta_dtype, "meta"));
+    if (scorer != QSKV_SCORE_BOUND && scorer != QSKV_SCORE_CENTROID)
+        return fail(QSKV_ERR_INVALID_ARG, "unknown scorer %d", int(scorer));
+    if (scorer == QSKV_SCORE_CENTROID && meta_dtype != QSKV_F32)
+        return fail(QSKV_ERR_INVALID_ARG, "centroid metadata is fp32");
+    if (!(epsilon >= 0.f && epsilon < 1.f)) return fail(QSKV_ERR_INVALID_ARG, "epsilon must be in [0, 1)");
+    if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
+    if (!q || !meta || !page_table || !seq_lens || !selected || !n_selected)
+        return fail(QSKV_ERR_INVALID_ARG, "q, meta, page_table, seq_lens, selected and n_selected must be non-NULL");
+    if (!aligned(q, 16) || !aligned(meta, 16)) return fail(QSKV_ERR_INVALID_ARG, "q and meta must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(scores, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and score arrays must be 4-byte aligned");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    SelectArgs a;
+    a.q = q;
+    a.meta = meta;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.scores = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = top_k;
+    a.need_max = int32_t(floor(double(epsilon) * double(top_k)));
+    a.seed = seed;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = scorer == QSKV_SCORE_CENTROID
+                              ? launch_page_select_centroid(a, q_dtype, shape->head_dim, st, scores != nullptr)
+                              : launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, st, scores != nullptr);
+    return launched(e, "page_select_approx launch");
 }
 
 qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,

@@ -316,6 +316,8 @@ struct SelectArgs {
     float *scores;          // [rows][max_pages]
     uint32_t *flags;
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages, top_k;
+    int32_t need_max;       // lossy top-K: stop refining once <= need_max keys are undecided (0: exact)
+    uint64_t seed;          // lossy top-K: seed of the sample's random start
 };
 
 struct DecodeArgs {

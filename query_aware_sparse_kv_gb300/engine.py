@@ -27,10 +27,15 @@ class PagedDecoder:
                 prefix attended once per KV head for the whole batch
     scorer      "bound" (TinyServe min/max metadata, the default) or
                 "centroid" (Block Top-K: fp32 mean key per page, q . centroid)
+    approx_epsilon  None: exact top-K; else the lossy top-K stops refining
+                once at most floor(epsilon * top_k) pages are undecided and
+                samples them from the threshold bucket (seed approx_seed)
     """
 
     def __init__(self, q, k_pool, v_pool, page_table, seq_lens, top_k: Optional[int], sm_scale: float = 0.0,
-                 prefix_pages: int = 0, scorer: str = "bound"):
+                 prefix_pages: int = 0, scorer: str = "bound", approx_epsilon: Optional[float] = None,
+                 approx_seed: int = 0):
+        self.approx_epsilon, self.approx_seed = approx_epsilon, approx_seed
         if scorer not in ("bound", "centroid"):
             raise ValueError(f"unknown scorer {scorer!r}")
         dev = k_pool.device
@@ -66,6 +71,11 @@ class PagedDecoder:
 
     # -- indexer phase -------------------------------------------------------
     def select(self, q=None, scores: Optional[torch.Tensor] = None, stream=None):
+        if self.approx_epsilon is not None:
+            B.page_select_approx(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k,
+                                 self.selected, self.n_selected, self.shape, self.workspace, self.approx_epsilon,
+                                 self.approx_seed, scorer=self.scorer, scores=scores, stream=stream)
+            return
         fn = B.page_select_centroid if self.scorer == "centroid" else B.page_select
         fn(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k, self.selected,
            self.n_selected, self.shape, self.workspace, scores, stream)
@@ -115,10 +125,11 @@ class PagedDecoder:
 
 
 def from_inputs(inputs: dict, device="cuda", top_k="spec", prefix_pages: int = 0,
-                scorer: str = "bound") -> PagedDecoder:
+                scorer: str = "bound", approx_epsilon: Optional[float] = None, approx_seed: int = 0) -> PagedDecoder:
     """A PagedDecoder over a workloads.make_inputs() batch copied to `device`."""
     if isinstance(top_k, str):
         top_k = inputs["top_k"]
     t = {k: inputs[k].to(device) for k in ("q", "k_pool", "v_pool", "page_table", "seq_lens")}
     return PagedDecoder(t["q"], t["k_pool"], t["v_pool"], t["page_table"], t["seq_lens"], top_k,
-                        prefix_pages=prefix_pages, scorer=scorer)
+                        prefix_pages=prefix_pages, scorer=scorer, approx_epsilon=approx_epsilon,
+                        approx_seed=approx_seed)
