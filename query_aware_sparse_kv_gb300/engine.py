@@ -102,19 +102,35 @@ class PagedDecoder:
             self.select(q, stream=stream)
         self.decode(q, stream=stream)
 
-    def capture_step(self, q: torch.Tensor, last_ids=None, last_valid=None):
+    def capture_step(self, q: torch.Tensor, last_ids=None, last_valid=None, q_host: Optional[torch.Tensor] = None,
+                     out_host: Optional[torch.Tensor] = None):
         """Record one step (metadata refresh, selection, decode) reading the
         query from the device buffer `q` into a CUDA graph, and return a
         function that replays it on the current stream.  Refill `q` in place
-        before each replay; results land in ``out`` / ``lse``."""
+        before each replay; results land in ``out`` / ``lse``.
+
+        With pinned host tensors ``q_host`` (shaped like q) and/or
+        ``out_host`` (shaped like out), the graph also copies the query in
+        from ``q_host`` first and the output back to ``out_host`` last, so a
+        serving loop launches one graph per step and synchronises once."""
+        def body():
+            if q_host is not None:
+                q.copy_(q_host, non_blocking=True)
+            self.step(q, last_ids, last_valid)
+            if out_host is not None:
+                out_host.copy_(self.out, non_blocking=True)
+
+        for t in (q_host, out_host):
+            if t is not None and not t.is_pinned():
+                raise ValueError("host buffers of a captured step must be pinned")
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            self.step(q, last_ids, last_valid)  # first use outside capture (device set-up)
+            body()  # first use outside capture (device set-up)
         torch.cuda.current_stream().wait_stream(side)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            self.step(q, last_ids, last_valid)
+            body()
         return graph.replay
 
     def check(self, stream=None):

@@ -247,3 +247,29 @@ def test_full_size_config_sampled(oracle_lib, name):
         sel = dec.selected
         assert (sel[..., 1:] > sel[..., :-1]).all()  # every row keeps >= top_k pages here
         assert (sel >= 0).all() and (sel < nb[:, None, None]).all()
+
+
+def test_captured_step_with_host_copies(oracle_lib):
+    """capture_step(q_host=, out_host=): one graph copies the query in from
+    pinned memory, runs the step and copies the output back; replays with two
+    different queries give the outputs of the direct calls."""
+    inp = W.make_inputs(SMALL["llama_small"])
+    dec = _run(inp, oracle_lib)
+    qv = W.q_variants(inp, 2)
+    want = []
+    for v in range(2):
+        dec.step(q=qv[v].cuda())
+        torch.cuda.synchronize()
+        want.append(dec.out.cpu().clone())
+    q_dev = torch.empty_like(dec.q)
+    out_host = torch.zeros(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    q_host = [qv[v].pin_memory() for v in range(2)]
+    graphs = [dec.capture_step(q_dev, q_host=q_host[v], out_host=out_host) for v in range(2)]
+    for v in (1, 0, 1):
+        out_host.zero_()
+        graphs[v]()
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(out_host, want[v])
+    dec.check()
+    with pytest.raises(ValueError):
+        dec.capture_step(q_dev, q_host=qv[0])  # not pinned
