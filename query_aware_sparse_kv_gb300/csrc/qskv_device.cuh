@@ -88,7 +88,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // start while the previous kernel in the stream drains.  pdl_wait() blocks
 // until that kernel has completed and its writes are visible; no kernel
 // touches global memory before it.  pdl_trigger() lets the next kernel in
-// the stream begin its own launch early.
+// the stream begin its own launch early; single-wave grids call it at entry,
+// the multi-wave scoring grids do not (their dependents would take SM
+// resources from their later waves).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
