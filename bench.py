@@ -216,6 +216,23 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------- oracle --
+def cpu_model() -> str:
+    """The host CPU's model name (x86 "model name", or Arm implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in info:
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    impl = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")]
+    part = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")]
+    if impl and part:
+        return f"Arm implementer {impl[0]} part {part[0]} x {len(part)}"
+    return "unknown"
+
+
 def oracle_sample(inputs: dict, qv_cpu, budget_s: float, threads: int, step_target_s: float | None = None,
                   scorer: str = "bound"):
     """Times the CPU oracle (scores, top-K, attention) on a bounded sample of
@@ -493,7 +510,10 @@ def run_gpu(args):
     if not args.no_cpu_baseline and world == 1:
         sps, cores, sample, _ = oracle_sample(inputs, qv_cpu, budget_s=args.cpu_budget,
                                               threads=os.cpu_count() or 1, scorer=args.scorer)
-        cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample}
+        sps1, _, sample1, _ = oracle_sample(inputs, qv_cpu, budget_s=max(1.0, args.cpu_budget / 4), threads=1,
+                                            scorer=args.scorer)
+        cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "single_thread": {"value": sps1, "unit": "steps/s", "sample": sample1}, "cpu_model": cpu_model()}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
