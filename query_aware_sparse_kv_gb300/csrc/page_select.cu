@@ -116,6 +116,7 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t i) {
 // Ranks one row's scores (all threads of the CTA take part).
 __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *srow) {
     constexpr int NT = kSelectThreads;
+    constexpr int NW = NT / 32;
     __shared__ uint32_t s_keys[kSelectKeyCap];
     __shared__ uint32_t s_hist[256];
     __shared__ int s_tmp[2 * NT / 32];
@@ -236,49 +237,111 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
     // (integer division; o = a SplitMix64 draw mod m): systematic sampling
     // with a random start, every bucket key kept with probability need / m.
     // Either way c(t) keys of the bucket precede bucket key t in the output.
-    const uint32_t thr = shr32(prefix, lo);
-    const int per = (n_b + NT - 1) / NT;
-    const int i0 = min(tid * per, n_b), i1 = min(i0 + per, n_b);
-    int cg = 0, ce = 0;
-    for (int i = i0; i < i1; i++) {
-        const uint32_t k = shr32(key_at(i), lo);
-        cg += k > thr;
-        ce += k == thr;
-    }
-    int gb = cg, eb = ce, m = 0;
-    block_exclusive_scan2<NT>(gb, eb, m, s_tmp);
-    const bool sampled = a.need_max > 0 && need < m;
-    if (!sampled) {
-        for (int i = i0; i < i1; i++) {
-            const uint32_t k = shr32(key_at(i), lo);
-            if (k > thr) {
-                const int pos = gb + min(eb, need);
-                if (pos < K) sel[pos] = i;
-                gb++;
-            } else if (k == thr) {
-                if (eb < need && gb + eb < K) sel[gb + eb] = i;
-                eb++;
+    if (n_b <= kSelectBallotKeys) {
+        // Warp w walks the contiguous keys [w0, w1) 32 at a time; ballot
+        // prefix counts give key i's gi / ei (keys above / in the bucket
+        // before it).  Measured faster than the per-thread runs below on
+        // rows of up to 2048 keys, slower on longer ones.
+        const uint32_t thr = shr32(prefix, lo);
+        const uint32_t lt = (1u << lane) - 1u;
+        const int cw = ((n_b + NW - 1) / NW + 31) & ~31;
+        const int w0 = min(warp * cw, n_b), w1 = min(w0 + cw, n_b);
+        int cg = 0, ce = 0;
+        for (int base = w0; base < w1; base += 32) {
+            const int i = base + lane;
+            const uint32_t k = i < w1 ? shr32(key_at(i), lo) : 0u;
+            cg += __popc(__ballot_sync(0xffffffffu, i < w1 && k > thr));
+            ce += __popc(__ballot_sync(0xffffffffu, i < w1 && k == thr));
+        }
+        if (lane == 0) {
+            s_tmp[warp] = cg;
+            s_tmp[NW + warp] = ce;
+        }
+        __syncthreads();
+        int gb = 0, eb = 0, m = 0;
+        for (int w = 0; w < NW; w++) {
+            if (w < warp) {
+                gb += s_tmp[w];
+                eb += s_tmp[NW + w];
             }
+            m += s_tmp[NW + w];
+        }
+        const bool sampled = a.need_max > 0 && need < m;
+        // t need + o < m (need + 1) < 2^32 here
+        const uint32_t o = sampled ? uint32_t(splitmix64(a.seed, uint64_t(row) + 1u) % uint64_t(m)) : 0u;
+        const int n_gt = K - need;               // keys above the bucket
+        const int eq_last = sampled ? m : need;  // bucket keys to walk past
+        for (int base = w0; base < w1; base += 32) {
+            if (gb >= n_gt && eb >= eq_last) break;  // every kept key is placed
+            const int i = base + lane;
+            const uint32_t k = i < w1 ? shr32(key_at(i), lo) : 0u;
+            const bool gt = i < w1 && k > thr, eq = i < w1 && k == thr;
+            const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+            const int gi = gb + __popc(bg & lt), ei = eb + __popc(be & lt);
+            if (!sampled) {
+                if (gt) {
+                    const int pos = gi + min(ei, need);
+                    if (pos < K) sel[pos] = i;
+                } else if (eq && ei < need && gi + ei < K) {
+                    sel[gi + ei] = i;
+                }
+            } else {
+                const uint32_t x = uint32_t(ei) * uint32_t(need) + o;
+                const int c = int(x / uint32_t(m));
+                if (gt) {
+                    if (gi + c < K) sel[gi + c] = i;
+                } else if (eq && int((x + uint32_t(need)) / uint32_t(m)) != c && gi + c < K) {
+                    sel[gi + c] = i;
+                }
+            }
+            gb += __popc(bg);
+            eb += __popc(be);
         }
     } else {
-        // c(t) and the remainder of (t need + o) by m, stepped per bucket key
-        // (t need + o < m (need + 1) < 2^32 for rows held in shared memory)
-        const uint64_t o = splitmix64(a.seed, uint64_t(row) + 1u) % uint64_t(m);
-        const uint64_t x = uint64_t(eb) * uint64_t(need) + o;
-        int c = int(x / uint64_t(m));
-        int rem = int(x - uint64_t(c) * uint64_t(m));
+        const uint32_t thr = shr32(prefix, lo);
+        const int per = (n_b + NT - 1) / NT;
+        const int i0 = min(tid * per, n_b), i1 = min(i0 + per, n_b);
+        int cg = 0, ce = 0;
         for (int i = i0; i < i1; i++) {
             const uint32_t k = shr32(key_at(i), lo);
-            if (k > thr) {
-                const int pos = gb + c;
-                if (pos < K) sel[pos] = i;
-                gb++;
-            } else if (k == thr) {
-                rem += need;
-                if (rem >= m) {  // c(t + 1) = c(t) + 1: this key is kept
-                    rem -= m;
-                    if (gb + c < K) sel[gb + c] = i;
-                    c++;
+            cg += k > thr;
+            ce += k == thr;
+        }
+        int gb = cg, eb = ce, m = 0;
+        block_exclusive_scan2<NT>(gb, eb, m, s_tmp);
+        const bool sampled = a.need_max > 0 && need < m;
+        if (!sampled) {
+            for (int i = i0; i < i1; i++) {
+                const uint32_t k = shr32(key_at(i), lo);
+                if (k > thr) {
+                    const int pos = gb + min(eb, need);
+                    if (pos < K) sel[pos] = i;
+                    gb++;
+                } else if (k == thr) {
+                    if (eb < need && gb + eb < K) sel[gb + eb] = i;
+                    eb++;
+                }
+            }
+        } else {
+            // c(t) and the remainder of (t need + o) by m, stepped per bucket key
+            // (t need + o < m (need + 1) < 2^32 for rows held in shared memory)
+            const uint64_t o = splitmix64(a.seed, uint64_t(row) + 1u) % uint64_t(m);
+            const uint64_t x = uint64_t(eb) * uint64_t(need) + o;
+            int c = int(x / uint64_t(m));
+            int rem = int(x - uint64_t(c) * uint64_t(m));
+            for (int i = i0; i < i1; i++) {
+                const uint32_t k = shr32(key_at(i), lo);
+                if (k > thr) {
+                    const int pos = gb + c;
+                    if (pos < K) sel[pos] = i;
+                    gb++;
+                } else if (k == thr) {
+                    rem += need;
+                    if (rem >= m) {  // c(t + 1) = c(t) + 1: this key is kept
+                        rem -= m;
+                        if (gb + c < K) sel[gb + c] = i;
+                        c++;
+                    }
                 }
             }
         }

@@ -395,6 +395,7 @@ __device__ __forceinline__ bool row_is_final(const DecodeArgs &a, int64_t w0, in
 constexpr int kScoreThreads = 128;    // scoring CTA: 4 warps x 32 pages
 constexpr int kSelectThreads = 256;   // ranking CTA: one row
 constexpr int kSelectKeyCap = 4096;   // keys held in shared memory by the select stage
+constexpr int kSelectBallotKeys = 2048;  // rows up to this long: warp-ballot compaction
 constexpr int kDecodeCtasPerSm = 2;   // decode grid = this x SM count
 // Decode pipeline shape per head dim: warps per CTA, 16-token halves per
 // stage, stages per warp (2 CTAs x warps x stages x stage bytes <= 227 KB).
