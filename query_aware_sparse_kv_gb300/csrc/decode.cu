@@ -158,6 +158,16 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     }
     __syncwarp();
     if (!a.wait_at_exit) pdl_wait();
+    // K/V streams larger than L2 are read evict-first; smaller ones with no
+    // hint (a hint with the normal policy measured slower than none)
+    const uint64_t kv_policy = l2_evict_first_policy();
+    const bool kv_hint = a.kv_evict_first != 0;
+    auto load_kv = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t *b) {
+        if (kv_hint)
+            tma_load_2d_hint(dst, map, x, y, b, kv_policy);
+        else
+            tma_load_2d(dst, map, x, y, b);
+    };
 
     // Units are walked with (row, slot) cursors, never by dividing the
     // 64-bit unit index in the loop.
@@ -239,14 +249,14 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                 mbar_arrive_expect_tx(bar + ps, uint32_t(nh) * 2 * HALF);
 #pragma unroll
                 for (int nb = 0; nb < NB; nb++) {
-                    tma_load_2d(st + nb * BOX, &tmap_k, nb * 64, y0, bar + ps);
-                    tma_load_2d(st + KVB + nb * BOX, &tmap_v, nb * 64, y0, bar + ps);
+                    load_kv(st + nb * BOX, &tmap_k, nb * 64, y0, bar + ps);
+                    load_kv(st + KVB + nb * BOX, &tmap_v, nb * 64, y0, bar + ps);
                 }
                 if (HALVES == 2 && nh == 2) {
 #pragma unroll
                     for (int nb = 0; nb < NB; nb++) {
-                        tma_load_2d(st + HALF + nb * BOX, &tmap_k, nb * 64, y1, bar + ps);
-                        tma_load_2d(st + KVB + HALF + nb * BOX, &tmap_v, nb * 64, y1, bar + ps);
+                        load_kv(st + HALF + nb * BOX, &tmap_k, nb * 64, y1, bar + ps);
+                        load_kv(st + KVB + HALF + nb * BOX, &tmap_v, nb * 64, y1, bar + ps);
                     }
                 }
             }
@@ -644,6 +654,14 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
                           int kv_dtype, int head_dim, const DecodeGrid &grid, cudaStream_t stream,
                           const PrefixArgs *prefix) {
     const bool qf = q_dtype == kDtypeF32;
+    // K/V this call may stream: when it exceeds L2 it is read evict-first, so
+    // it does not push the split partials, scores and tables out of L2; a
+    // smaller selection is left to stay in L2 for the next step.
+    DecodeArgs da = a;
+    const int l2 = l2_cache_bytes();
+    const double kv_bytes =
+        double(a.total_units) * a.page_size * head_dim * 2.0 * (kv_dtype == kDtypeBf16 ? 2.0 : 4.0);
+    da.kv_evict_first = l2 > 0 && kv_bytes > double(l2) ? 1 : 0;
     if (prefix) {
         // cascade: the shared prefix first; it waits for the previous kernel
         // and then releases the decode of the rows' own pages, which runs on
@@ -654,7 +672,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
         cudaError_t e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
         if (e != cudaSuccess) return e;
         if (a.total_units > 0) {
-            DecodeArgs d = a;
+            DecodeArgs d = da;
             d.wait_at_exit = 1;
             if (head_dim == 128)
                 e = qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream)
@@ -670,11 +688,11 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
     if (kv_dtype == kDtypeBf16) {
         cudaError_t e;
         if (head_dim == 128)
-            e = qf ? launch_bf16<128, true>(a, tmap_k, tmap_v, grid, stream)
-                   : launch_bf16<128, false>(a, tmap_k, tmap_v, grid, stream);
+            e = qf ? launch_bf16<128, true>(da, tmap_k, tmap_v, grid, stream)
+                   : launch_bf16<128, false>(da, tmap_k, tmap_v, grid, stream);
         else
-            e = qf ? launch_bf16<64, true>(a, tmap_k, tmap_v, grid, stream)
-                   : launch_bf16<64, false>(a, tmap_k, tmap_v, grid, stream);
+            e = qf ? launch_bf16<64, true>(da, tmap_k, tmap_v, grid, stream)
+                   : launch_bf16<64, false>(da, tmap_k, tmap_v, grid, stream);
         if (e != cudaSuccess) return e;
         return launch_merge(a, head_dim, stream);
     }

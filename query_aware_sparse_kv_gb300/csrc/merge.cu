@@ -42,8 +42,10 @@ __device__ __forceinline__ void fold_range(Fold &f, const float *lse_p, const fl
         for (int j = 0; j < SC; j++) {
             const int sidx = s0 + j * stride;
             const bool ok = sidx < n;
+            // o is loaded with its lse (one round trip); an empty piece's o
+            // (never written) is loaded too but not used
             l[j] = ok ? __ldcg(lse_p + int64_t(sidx) * lse_step) : -INFINITY;
-            v[j] = ok && l[j] != -INFINITY ? __ldcg(o_p + int64_t(sidx) * o_step) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = ok ? __ldcg(o_p + int64_t(sidx) * o_step) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float m = f.mx;
 #pragma unroll
@@ -57,7 +59,7 @@ __device__ __forceinline__ void fold_range(Fold &f, const float *lse_p, const fl
         f.acc.w *= sc;
 #pragma unroll
         for (int j = 0; j < SC; j++) {
-            if (l[j] == -INFINITY) continue;  // an empty piece: its o was never written
+            if (l[j] == -INFINITY) continue;  // an empty piece: its o holds no data
             const float w = exp2f(l[j] - m);
             f.den += w;
             f.acc.x = fmaf(w, v[j].x, f.acc.x);

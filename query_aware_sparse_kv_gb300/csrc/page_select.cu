@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a) {
 // ---------------------------------------------- scores on tensor cores --
 // Three CTAs per SM (168 registers): more metadata rows in flight per SM than
 // at two, measured faster on GB300 despite a small spill.
-template <int D, bool QF32>
+// HINT: the metadata scan is larger than L2 and is read evict-first.
+template <int D, bool QF32, bool HINT>
 __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
     constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
     const RowInfo r = row_info(a);
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
         pp[i] = vv[i] ? trow[jj[i]] : 0;
     }
     const char *meta = static_cast<const char *>(a.meta);
+    const uint64_t meta_policy = HINT ? l2_evict_first_policy() : 0;
     uint4 av[4][NKP];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
@@ -409,7 +411,9 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
         const char *rowp = meta + (int64_t(bad[i] ? 0 : pp[i]) * a.num_kv_heads + r.g) * (2 * D * 2);
 #pragma unroll
         for (int kp = 0; kp < NKP; kp++)
-            av[i][kp] = (vv[i] && !bad[i]) ? ldg_stream_v4(rowp + (4 * kp + t) * 16) : make_uint4(0, 0, 0, 0);
+            av[i][kp] = !(vv[i] && !bad[i]) ? make_uint4(0, 0, 0, 0)
+                        : HINT ? ldg_stream_v4_hint(rowp + (4 * kp + t) * 16, meta_policy)
+                               : ldg_stream_v4(rowp + (4 * kp + t) * 16);
     }
     if ((bad[0] || bad[1] || bad[2] || bad[3]) && t == 0) raise_error(a.flags, kErrPageId);
 
@@ -647,20 +651,30 @@ cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int he
     return launch_pdl(select_kernel, dim3(unsigned(rows)), dim3(kSelectThreads), 0, stream, a);
 }
 
-cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
-                               int score_all) {
-    const int64_t rows = int64_t(a.batch) * a.num_kv_heads;
+cudaError_t launch_page_select(const SelectArgs &a_in, int q_dtype, int meta_dtype, int head_dim,
+                               cudaStream_t stream, int score_all) {
+    const int64_t rows = int64_t(a_in.batch) * a_in.num_kv_heads;
+    // a metadata scan larger than L2 is read evict-first (see launch_decode)
+    SelectArgs a = a_in;
+    const int l2 = l2_cache_bytes();
+    const double meta_bytes = double(rows) * a.max_pages * 2.0 * head_dim * (meta_dtype == kDtypeBf16 ? 2.0 : 4.0);
+    a.meta_evict_first = l2 > 0 && meta_bytes > double(l2) ? 1 : 0;
     const dim3 grid(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
     const dim3 block(kScoreThreads);
     const bool qf = q_dtype == kDtypeF32;
     cudaError_t e;
     if (meta_dtype == kDtypeBf16) {
+        const bool h = a.meta_evict_first != 0;
         if (head_dim == 128)
-            e = qf ? launch_pdl(score_mma_kernel<128, true>, grid, block, 0, stream, a, score_all)
-                   : launch_pdl(score_mma_kernel<128, false>, grid, block, 0, stream, a, score_all);
+            e = qf ? (h ? launch_pdl(score_mma_kernel<128, true, true>, grid, block, 0, stream, a, score_all)
+                        : launch_pdl(score_mma_kernel<128, true, false>, grid, block, 0, stream, a, score_all))
+                   : (h ? launch_pdl(score_mma_kernel<128, false, true>, grid, block, 0, stream, a, score_all)
+                        : launch_pdl(score_mma_kernel<128, false, false>, grid, block, 0, stream, a, score_all));
         else
-            e = qf ? launch_pdl(score_mma_kernel<64, true>, grid, block, 0, stream, a, score_all)
-                   : launch_pdl(score_mma_kernel<64, false>, grid, block, 0, stream, a, score_all);
+            e = qf ? (h ? launch_pdl(score_mma_kernel<64, true, true>, grid, block, 0, stream, a, score_all)
+                        : launch_pdl(score_mma_kernel<64, true, false>, grid, block, 0, stream, a, score_all))
+                   : (h ? launch_pdl(score_mma_kernel<64, false, true>, grid, block, 0, stream, a, score_all)
+                        : launch_pdl(score_mma_kernel<64, false, false>, grid, block, 0, stream, a, score_all));
     } else {
         e = qf ? launch_pdl(score_simt_kernel<float, true>, grid, block, 0, stream, a, head_dim, score_all)
                : launch_pdl(score_simt_kernel<float, false>, grid, block, 0, stream, a, head_dim, score_all);

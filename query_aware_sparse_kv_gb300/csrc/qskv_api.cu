@@ -41,6 +41,17 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
     return w;
 }
 
+int l2_cache_bytes() {
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 128) cache[dev] = n;
+    return n;
+}
+
 }  // namespace qskv
 
 using namespace qskv;
@@ -248,6 +259,7 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     a.top_k = top_k;
     a.need_max = 0;
     a.seed = 0;
+    a.meta_evict_first = 0;
     return launched(launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                        scores != nullptr),
                     "page_select launch");
@@ -322,6 +334,7 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
     a.top_k = top_k;
     a.need_max = 0;
     a.seed = 0;
+    a.meta_evict_first = 0;
     return launched(launch_page_select_centroid(a, q_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                                 scores != nullptr),
                     "page_select_centroid launch");
@@ -373,6 +386,7 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
     a.top_k = top_k;
     a.need_max = int32_t(floor(double(epsilon) * double(top_k)));
     a.seed = seed;
+    a.meta_evict_first = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = scorer == QSKV_SCORE_CENTROID
                               ? launch_page_select_centroid(a, q_dtype, shape->head_dim, st, scores != nullptr)
@@ -433,6 +447,7 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     a.extra_pieces = 0;
     a.extra_slot0 = 0;
     a.wait_at_exit = 0;
+    a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -519,6 +534,7 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     a.extra_pieces = 0;
     a.extra_slot0 = 0;
     a.wait_at_exit = 0;
+    a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
@@ -607,6 +623,7 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     a.extra_pieces = E;
     a.extra_slot0 = rows + grid.total_warps;
     a.wait_at_exit = 0;
+    a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;

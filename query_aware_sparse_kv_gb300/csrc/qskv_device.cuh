@@ -122,6 +122,27 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// L2 policy for data read once per step (the KV stream of the decode, the
+// page metadata of the scan): its lines are evicted first, so the stream
+// does not push out of L2 the small buffers the next kernel reads (scores,
+// split partials, page tables).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Asks L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned global address.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
@@ -298,6 +319,15 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     return v;
 }
 
+// ldg_stream_v4 with an L2 cache policy.
+__device__ __forceinline__ uint4 ldg_stream_v4_hint(const void *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 // ------------------------------------------------------- kernel arguments --
 struct MetaArgs {
     const void *k_pool;
@@ -320,6 +350,7 @@ struct SelectArgs {
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages, top_k;
     int32_t need_max;       // lossy top-K: stop refining once <= need_max keys are undecided (0: exact)
     uint64_t seed;          // lossy top-K: seed of the sample's random start
+    int32_t meta_evict_first;  // 1: the metadata scan exceeds L2, read it evict-first
 };
 
 struct DecodeArgs {
@@ -341,6 +372,7 @@ struct DecodeArgs {
     int32_t extra_pieces;   // partials per row written by another kernel (0: none)
     int64_t extra_slot0;    // row r's extra piece e sits in slot extra_slot0 + r * extra_pieces + e
     int32_t wait_at_exit;   // 1: wait for the previous grid at exit, not before the first access
+    int32_t kv_evict_first; // 1: this call's K/V stream exceeds L2, read it evict-first
                             // (the previous grid is the cascade's prefix kernel, which itself
                             // waited for everything before it)
     int32_t stages;

@@ -34,6 +34,8 @@ struct DecodeGrid {
 };
 
 DecodeGrid decode_grid(int num_sms, int head_dim);
+// L2 bytes of the current device (cached per device; 0 if it cannot be read).
+int l2_cache_bytes();
 // extra_per_row: partial slots per row for the shared-prefix pieces of a
 // cascade decode (0 otherwise).
 WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_pages, int num_sms,
