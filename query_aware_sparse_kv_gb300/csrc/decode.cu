@@ -118,7 +118,9 @@ __device__ void write_empty_piece(const DecodeArgs &a, int row, int64_t gw) {
 
 // A stage holds up to HALVES 16-token sub-tiles ("halves") of one row: K
 // then V, each half as D/64 boxes of 16 tokens x 64 dims (128-byte swizzle).
-template <int D, bool QF32, int WPC, int HALVES>
+// HINT: the call streams more K/V than L2 holds; the loads carry an
+// evict-first L2 policy.
+template <int D, bool QF32, int WPC, int HALVES, bool HINT>
 __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        DecodeArgs a) {
@@ -159,11 +161,11 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     __syncwarp();
     if (!a.wait_at_exit) pdl_wait();
     // K/V streams larger than L2 are read evict-first; smaller ones with no
-    // hint (a hint with the normal policy measured slower than none)
-    const uint64_t kv_policy = l2_evict_first_policy();
-    const bool kv_hint = a.kv_evict_first != 0;
+    // hint (a hint with the normal policy, or a branch on the choice in the
+    // issue path, measured slower than plain loads)
+    const uint64_t kv_policy = HINT ? l2_evict_first_policy() : 0;
     auto load_kv = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t *b) {
-        if (kv_hint)
+        if constexpr (HINT)
             tma_load_2d_hint(dst, map, x, y, b, kv_policy);
         else
             tma_load_2d(dst, map, x, y, b);
@@ -594,14 +596,14 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
     if (cur_row >= 0) finish_row(cur_row);
 }
 
-template <int D, bool QF32>
-cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
-                        cudaStream_t stream) {
+template <int D, bool QF32, bool HINT>
+cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                             const DecodeGrid &grid, cudaStream_t stream) {
     constexpr int WPC = D == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64;
     constexpr int HALVES = D == 128 ? kDecodeHalvesD128 : kDecodeHalvesD64;
     if (grid.warps_per_cta != WPC) return cudaErrorInvalidConfiguration;
     const size_t smem = decode_smem_bytes(D, a.stages);
-    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES>;
+    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -611,6 +613,13 @@ cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtens
         if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
     return launch_pdl(kernel, dim3(grid.ctas), dim3(WPC * 32), smem, stream, *tk, *tv, a);
+}
+
+template <int D, bool QF32>
+cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
+                        cudaStream_t stream) {
+    return a.kv_evict_first ? launch_bf16_hint<D, QF32, true>(a, tk, tv, grid, stream)
+                            : launch_bf16_hint<D, QF32, false>(a, tk, tv, grid, stream);
 }
 
 }  // namespace
@@ -656,12 +665,15 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
     const bool qf = q_dtype == kDtypeF32;
     // K/V this call may stream: when it exceeds L2 it is read evict-first, so
     // it does not push the split partials, scores and tables out of L2; a
-    // smaller selection is left to stay in L2 for the next step.
+    // smaller selection is left to stay in L2 for the next step.  A plain
+    // dense decode keeps the normal policy: its rows may alias pages (a
+    // shared prefix in the block table), which L2 then serves to every row.
     DecodeArgs da = a;
     const int l2 = l2_cache_bytes();
     const double kv_bytes =
         double(a.total_units) * a.page_size * head_dim * 2.0 * (kv_dtype == kDtypeBf16 ? 2.0 : 4.0);
-    da.kv_evict_first = l2 > 0 && kv_bytes > double(l2) ? 1 : 0;
+    const bool private_pages = a.selected != nullptr || a.page_begin > 0;
+    da.kv_evict_first = private_pages && l2 > 0 && kv_bytes > double(l2) ? 1 : 0;
     if (prefix) {
         // cascade: the shared prefix first; it waits for the previous kernel
         // and then releases the decode of the rows' own pages, which runs on
