@@ -478,10 +478,11 @@ def run_gpu(args):
     value = world * args.steps / (elapsed_ms / 1000.0)
 
     # end to end through the public API: each step is one replay of a graph
-    # captured by PagedDecoder.capture_step with the host buffers: it copies
-    # the step's query in from pinned host memory, runs the step and copies
-    # the output back to pinned host memory; the host waits for it before
-    # the next step (a serving loop needs the output to go on).
+    # captured by PagedDecoder.capture_step with the host buffers: its
+    # kernels read the step's query from pinned host memory and write the
+    # output into pinned host memory (zero-copy over the host link); the host
+    # waits for it before the next step (a serving loop needs the output to
+    # go on).
     e2e_steps = 0 if args.no_e2e else min(args.steps, 500)
     q_host = qv_cpu.pin_memory()
     q_dev = torch.empty_like(qv[0])
@@ -531,7 +532,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "step_launch": "CUDA graph replay, one graph per query variant (meta refresh + selection + decode)",
         "eager_ms_per_step": eager_ms,
-        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: H2D + step + D2H in one graph, host sync per step",
+        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to pinned host memory (zero-copy), host sync per step",
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
         # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking;

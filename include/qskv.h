@@ -35,7 +35,10 @@
  *   Vortex digest, method overview item 1 (per-block mean keys scored by q,
  *   "Block Top-K").
  *
- * Layouts (row-major, all on the device unless stated):
+ * Layouts (row-major, all on the device unless stated; q, out and lse may
+ * also be pinned host memory the device can address, which the kernels then
+ * read and write directly, e.g. over GB300's NVLink-C2C host link; q, out
+ * and lse are only read or written with plain loads and stores):
  *   k_pool, v_pool  [num_pool_pages][num_kv_heads][page_size][head_dim]  (kv dtype)
  *   meta            [num_pool_pages][num_kv_heads][2][head_dim]          (kv dtype)
  *                   row 0 = element-wise min m, row 1 = max M, over the

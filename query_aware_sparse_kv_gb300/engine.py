@@ -94,26 +94,36 @@ class PagedDecoder:
                               top_k=self.top_k or 0, lse=self.lse if lse is None else lse, sm_scale=self.sm_scale,
                               stream=stream)
 
-    def step(self, q=None, last_ids=None, last_valid=None, stream=None):
-        """Metadata refresh of the pages being appended to, selection, decode."""
+    def step(self, q=None, last_ids=None, last_valid=None, stream=None, out=None):
+        """Metadata refresh of the pages being appended to, selection, decode
+        (into ``out`` if given, else ``self.out``)."""
         if last_ids is not None:
             self.build_meta(last_ids, last_valid, stream)
         if self.top_k is not None:
             self.select(q, stream=stream)
-        self.decode(q, stream=stream)
+        self.decode(q, out=out, stream=stream)
 
     def capture_step(self, q: torch.Tensor, last_ids=None, last_valid=None, q_host: Optional[torch.Tensor] = None,
-                     out_host: Optional[torch.Tensor] = None):
+                     out_host: Optional[torch.Tensor] = None, zero_copy: bool = True):
         """Record one step (metadata refresh, selection, decode) reading the
         query from the device buffer `q` into a CUDA graph, and return a
         function that replays it on the current stream.  Refill `q` in place
         before each replay; results land in ``out`` / ``lse``.
 
         With pinned host tensors ``q_host`` (shaped like q) and/or
-        ``out_host`` (shaped like out), the graph also copies the query in
-        from ``q_host`` first and the output back to ``out_host`` last, so a
-        serving loop launches one graph per step and synchronises once."""
+        ``out_host`` (shaped like out) the graph also moves the query in and
+        the output out, so a serving loop launches one graph per step and
+        synchronises once.  zero_copy=True (default): the kernels read the
+        query straight from ``q_host`` and write the output straight into
+        ``out_host`` (pinned host memory is device-accessible; on GB300 the
+        NVLink-C2C link makes this faster than copy nodes); refill ``q_host``
+        before each replay, and ``out`` is not written.  zero_copy=False: copy
+        nodes from ``q_host`` into ``q`` first and from ``out`` into
+        ``out_host`` last."""
         def body():
+            if zero_copy:
+                self.step(q if q_host is None else q_host, last_ids, last_valid, out=out_host)
+                return
             if q_host is not None:
                 q.copy_(q_host, non_blocking=True)
             self.step(q, last_ids, last_valid)
@@ -123,6 +133,10 @@ class PagedDecoder:
         for t in (q_host, out_host):
             if t is not None and not t.is_pinned():
                 raise ValueError("host buffers of a captured step must be pinned")
+        if q_host is not None and (q_host.shape != q.shape or q_host.dtype != q.dtype):
+            raise ValueError("q_host must have the shape and dtype of q")
+        if out_host is not None and (out_host.shape != self.out.shape or out_host.dtype != self.out.dtype):
+            raise ValueError("out_host must have the shape and dtype of out")
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):

@@ -249,9 +249,11 @@ def test_full_size_config_sampled(oracle_lib, name):
         assert (sel >= 0).all() and (sel < nb[:, None, None]).all()
 
 
-def test_captured_step_with_host_copies(oracle_lib):
-    """capture_step(q_host=, out_host=): one graph copies the query in from
-    pinned memory, runs the step and copies the output back; replays with two
+@pytest.mark.parametrize("zero_copy", [True, False])
+def test_captured_step_with_host_copies(oracle_lib, zero_copy):
+    """capture_step(q_host=, out_host=): one graph takes the query from pinned
+    memory, runs the step and puts the output in pinned memory (the kernels
+    reading and writing host memory directly, or copy nodes); replays with two
     different queries give the outputs of the direct calls."""
     inp = W.make_inputs(SMALL["llama_small"])
     dec = _run(inp, oracle_lib)
@@ -264,7 +266,7 @@ def test_captured_step_with_host_copies(oracle_lib):
     q_dev = torch.empty_like(dec.q)
     out_host = torch.zeros(dec.out.shape, dtype=dec.out.dtype).pin_memory()
     q_host = [qv[v].pin_memory() for v in range(2)]
-    graphs = [dec.capture_step(q_dev, q_host=q_host[v], out_host=out_host) for v in range(2)]
+    graphs = [dec.capture_step(q_dev, q_host=q_host[v], out_host=out_host, zero_copy=zero_copy) for v in range(2)]
     for v in (1, 0, 1):
         out_host.zero_()
         graphs[v]()
@@ -273,3 +275,5 @@ def test_captured_step_with_host_copies(oracle_lib):
     dec.check()
     with pytest.raises(ValueError):
         dec.capture_step(q_dev, q_host=qv[0])  # not pinned
+    with pytest.raises(ValueError):
+        dec.capture_step(q_dev, q_host=qv[0][:1].pin_memory())  # wrong shape
