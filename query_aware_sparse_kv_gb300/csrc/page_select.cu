@@ -541,7 +541,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_simt_kernel(SelectArgs a,
 // head) partial dot products of a batch are reduced with one butterfly
 // reduce-scatter (31 shuffles; lane l ends with the total of (page l / G,
 // head l % G)), then a max over each group of G lanes.
-template <int D, bool QF32, int G>
+// HINT: the centroid scan is larger than L2 and is read evict-first.
+template <int D, bool QF32, int G, bool HINT>
 __global__ void __launch_bounds__(kScoreThreads) score_centroid_kernel(SelectArgs a, int score_all) {
     constexpr int VEC = D / 32;  // dims per lane
     constexpr int NPG = 32 / G;  // pages per batch
@@ -573,6 +574,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_centroid_kernel(SelectArg
         }
     }
     const float *cent = static_cast<const float *>(a.meta);
+    const uint64_t policy = HINT ? l2_evict_first_policy() : 0;
     for (int p0 = 0; p0 < 32 && w_page0 + p0 < r.n_b; p0 += NPG) {
         // loads of the batch's pages first
         float c[NPG][VEC];
@@ -581,13 +583,30 @@ __global__ void __launch_bounds__(kScoreThreads) score_centroid_kernel(SelectArg
             const int pk = __shfl_sync(0xffffffffu, pid, p0 + k);
             const float *row = cent + (int64_t(pk < 0 ? 0 : pk) * a.num_kv_heads + r.g) * D + lane * VEC;
             if (VEC == 4) {
-                const float4 x = pk >= 0 ? __ldg(reinterpret_cast<const float4 *>(row)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (pk >= 0) {
+                    if constexpr (HINT) {
+                        const uint4 u = ldg_stream_v4_hint(row, policy);
+                        x = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                        __uint_as_float(u.w));
+                    } else {
+                        x = __ldg(reinterpret_cast<const float4 *>(row));
+                    }
+                }
                 c[k][0] = x.x;
                 c[k][VEC > 1 ? 1 : 0] = x.y;
                 c[k][VEC > 2 ? 2 : 0] = x.z;
                 c[k][VEC > 3 ? 3 : 0] = x.w;
             } else {
-                const float2 x = pk >= 0 ? __ldg(reinterpret_cast<const float2 *>(row)) : make_float2(0.f, 0.f);
+                float2 x = make_float2(0.f, 0.f);
+                if (pk >= 0) {
+                    if constexpr (HINT) {
+                        const uint2 u = ldg_stream_v2_hint(row, policy);
+                        x = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+                    } else {
+                        x = __ldg(reinterpret_cast<const float2 *>(row));
+                    }
+                }
                 c[k][0] = x.x;
                 c[k][VEC > 1 ? 1 : 0] = x.y;
             }
@@ -630,23 +649,30 @@ cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int he
     const dim3 grid(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
     const dim3 block(kScoreThreads);
     const bool qf = q_dtype == kDtypeF32;
+    // a centroid scan larger than L2 is read evict-first (see launch_decode)
+    const int l2 = l2_cache_bytes();
+    const bool hint = l2 > 0 && double(rows) * a.max_pages * head_dim * 4.0 > double(l2);
     cudaError_t e = cudaErrorInvalidValue;
-    auto go = [&](auto d_tag, auto q_tag) {
+    auto go = [&](auto d_tag, auto q_tag, auto h_tag) {
         constexpr int D = decltype(d_tag)::value;
         constexpr bool QF = decltype(q_tag)::value;
+        constexpr bool H = decltype(h_tag)::value;
         switch (a.group) {
-            case 1: e = launch_pdl(score_centroid_kernel<D, QF, 1>, grid, block, 0, stream, a, score_all); break;
-            case 2: e = launch_pdl(score_centroid_kernel<D, QF, 2>, grid, block, 0, stream, a, score_all); break;
-            case 4: e = launch_pdl(score_centroid_kernel<D, QF, 4>, grid, block, 0, stream, a, score_all); break;
-            case 8: e = launch_pdl(score_centroid_kernel<D, QF, 8>, grid, block, 0, stream, a, score_all); break;
+            case 1: e = launch_pdl(score_centroid_kernel<D, QF, 1, H>, grid, block, 0, stream, a, score_all); break;
+            case 2: e = launch_pdl(score_centroid_kernel<D, QF, 2, H>, grid, block, 0, stream, a, score_all); break;
+            case 4: e = launch_pdl(score_centroid_kernel<D, QF, 4, H>, grid, block, 0, stream, a, score_all); break;
+            case 8: e = launch_pdl(score_centroid_kernel<D, QF, 8, H>, grid, block, 0, stream, a, score_all); break;
         }
+    };
+    auto go_h = [&](auto d_tag, auto q_tag) {
+        hint ? go(d_tag, q_tag, std::true_type()) : go(d_tag, q_tag, std::false_type());
     };
     using I64 = std::integral_constant<int, 64>;
     using I128 = std::integral_constant<int, 128>;
     if (head_dim == 128)
-        qf ? go(I128(), std::true_type()) : go(I128(), std::false_type());
+        qf ? go_h(I128(), std::true_type()) : go_h(I128(), std::false_type());
     else
-        qf ? go(I64(), std::true_type()) : go(I64(), std::false_type());
+        qf ? go_h(I64(), std::true_type()) : go_h(I64(), std::false_type());
     if (e != cudaSuccess) return e;
     return launch_pdl(select_kernel, dim3(unsigned(rows)), dim3(kSelectThreads), 0, stream, a);
 }

@@ -319,6 +319,15 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     return v;
 }
 
+// 8-byte streaming load with an L2 cache policy.
+__device__ __forceinline__ uint2 ldg_stream_v2_hint(const void *p, uint64_t policy) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 // ldg_stream_v4 with an L2 cache policy.
 __device__ __forceinline__ uint4 ldg_stream_v4_hint(const void *p, uint64_t policy) {
     uint4 v;

@@ -249,6 +249,38 @@ def test_full_size_config_sampled(oracle_lib, name):
         assert (sel >= 0).all() and (sel < nb[:, None, None]).all()
 
 
+@pytest.mark.parametrize("case", ["centroid_lossy", "cascade"])
+def test_zero_copy_step_matches_the_device_path(oracle_lib, case):
+    """The zero-copy captured step (kernels reading q from and writing out to
+    pinned host memory) gives bit-identical outputs to the device-resident
+    calls, for the Block Top-K scorer with the lossy top-K and for the
+    shared-prefix cascade (whose prefix kernel reads q too)."""
+    if case == "cascade":
+        spec = W.spec_for("shared_prefix", batch=6, prefix_pages=9, suffix_pages=4)
+        inp = W.make_inputs(spec)
+        dec = qskv.from_inputs(inp, top_k=None, prefix_pages=9)
+    else:
+        inp = W.make_inputs(SMALL["long_small"])
+        dec = qskv.from_inputs(inp, scorer="centroid", approx_epsilon=0.05, approx_seed=4)
+        ids, vt = oracle_lib.all_pages(inp)
+        dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    qv = W.q_variants(inp, 2)
+    want = []
+    for v in range(2):
+        dec.step(q=qv[v].cuda())
+        torch.cuda.synchronize()
+        want.append(dec.out.cpu().clone())
+    q_host = [qv[v].pin_memory() for v in range(2)]
+    out_host = torch.zeros(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    graphs = [dec.capture_step(torch.empty_like(dec.q), q_host=q_host[v], out_host=out_host) for v in range(2)]
+    for v in (0, 1, 0):
+        out_host.zero_()
+        graphs[v]()
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(out_host, want[v])
+    dec.check()
+
+
 @pytest.mark.parametrize("zero_copy", [True, False])
 def test_captured_step_with_host_copies(oracle_lib, zero_copy):
     """capture_step(q_host=, out_host=): one graph takes the query from pinned
