@@ -69,6 +69,30 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
     return r;
 }
 
+// Head-major grid of the bound scan (num_kv_heads a multiple of 4): CTA
+// (x, b) covers the 32 pages from 32 (x / Q) of sequence b for KV heads
+// 4 (x % Q) .. 4 (x % Q) + 3, one head per warp (Q = num_kv_heads / 4), so
+// the CTAs x .. x + Q - 1, launched back to back, read a page's metadata rows
+// for all heads (contiguous in the [page][head] layout) at about the same
+// time.  page0: the warp's first page.
+__device__ __forceinline__ RowInfo row_info_head_major(const SelectArgs &a, int &page0) {
+    pdl_wait();
+    RowInfo r;
+    const int warp = threadIdx.x >> 5;
+    r.b = blockIdx.y;
+    r.g = (blockIdx.x % a.head_quads) * 4 + warp;
+    r.row = r.b * a.num_kv_heads + r.g;
+    page0 = (blockIdx.x / a.head_quads) * 32;
+    int seq = a.seq_lens[r.b];
+    const int cap = a.max_pages * a.page_size;
+    if (seq < 0 || seq > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
+        seq = seq < 0 ? 0 : cap;
+    }
+    r.n_b = (seq + a.page_size - 1) / a.page_size;
+    return r;
+}
+
 // --------------------------------------------------------------- select --
 // Exclusive block scans of x and y; total_y gets the sum of y over the block.
 template <int NT>
@@ -369,11 +393,17 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a) {
 template <int D, bool QF32, bool HINT>
 __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
     constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
-    const RowInfo r = row_info(a);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = lane & 3, gid = lane >> 2;
+    int w_page0;  // this warp's 32 pages: 2 groups of 16
+    RowInfo r;
+    if (a.head_quads > 0) {
+        r = row_info_head_major(a, w_page0);
+    } else {
+        r = row_info(a);
+        w_page0 = blockIdx.x * kScoreThreads + warp * 32;
+    }
     float *srow = a.scores + int64_t(r.row) * a.max_pages;
-    const int w_page0 = blockIdx.x * kScoreThreads + warp * 32;  // this warp's 32 pages: 2 groups of 16
     if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
 
     // Every load of the warp is issued before any is used: q, the page ids,
@@ -685,7 +715,10 @@ cudaError_t launch_page_select(const SelectArgs &a_in, int q_dtype, int meta_dty
     const int l2 = l2_cache_bytes();
     const double meta_bytes = double(rows) * a.max_pages * 2.0 * head_dim * (meta_dtype == kDtypeBf16 ? 2.0 : 4.0);
     a.meta_evict_first = l2 > 0 && meta_bytes > double(l2) ? 1 : 0;
-    const dim3 grid(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
+    a.head_quads = meta_dtype == kDtypeBf16 && a.num_kv_heads % 4 == 0 ? a.num_kv_heads / 4 : 0;
+    const dim3 grid = a.head_quads > 0
+                          ? dim3(unsigned((a.max_pages + 31) / 32 * a.head_quads), unsigned(a.batch))
+                          : dim3(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
     const dim3 block(kScoreThreads);
     const bool qf = q_dtype == kDtypeF32;
     cudaError_t e;

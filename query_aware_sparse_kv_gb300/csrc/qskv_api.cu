@@ -260,6 +260,7 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     a.need_max = 0;
     a.seed = 0;
     a.meta_evict_first = 0;
+    a.head_quads = 0;
     return launched(launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                        scores != nullptr),
                     "page_select launch");
@@ -335,6 +336,7 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
     a.need_max = 0;
     a.seed = 0;
     a.meta_evict_first = 0;
+    a.head_quads = 0;
     return launched(launch_page_select_centroid(a, q_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                                 scores != nullptr),
                     "page_select_centroid launch");
@@ -387,6 +389,7 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
     a.need_max = int32_t(floor(double(epsilon) * double(top_k)));
     a.seed = seed;
     a.meta_evict_first = 0;
+    a.head_quads = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = scorer == QSKV_SCORE_CENTROID
                               ? launch_page_select_centroid(a, q_dtype, shape->head_dim, st, scores != nullptr)

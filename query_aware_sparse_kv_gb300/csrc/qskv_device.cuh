@@ -360,6 +360,7 @@ struct SelectArgs {
     int32_t need_max;       // lossy top-K: stop refining once <= need_max keys are undecided (0: exact)
     uint64_t seed;          // lossy top-K: seed of the sample's random start
     int32_t meta_evict_first;  // 1: the metadata scan exceeds L2, read it evict-first
+    int32_t head_quads;     // bound scan: > 0 selects the head-major grid (num_kv_heads / 4)
 };
 
 struct DecodeArgs {
