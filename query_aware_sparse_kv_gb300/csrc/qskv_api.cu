@@ -596,7 +596,14 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     const int E = prefix_splits(shape->batch, G, shape->num_kv_heads, shape->page_size, prefix_pages, sms);
     const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms, E);
     QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
-    const DecodeGrid grid = decode_grid(sms, shape->head_dim);
+    // The prefix runs as a persistent grid on a share of the SMs and the
+    // paged decode of the rows' own pages on the others, side by side.  The
+    // partial slots keep the full grid's layout (prefix pieces after every
+    // decode warp's slot).
+    const DecodeGrid full = decode_grid(sms, shape->head_dim);
+    const int prefix_items = E > 0 ? prefix_tiles(shape->batch, G) * shape->num_kv_heads * E : 0;
+    const int pctas = prefix_ctas(prefix_items, sms);
+    const DecodeGrid grid = decode_grid(sms - pctas > 0 ? sms - pctas : 1, shape->head_dim);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
 
@@ -624,7 +631,7 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     a.page_begin = E > 0 ? prefix_pages : 0;
     a.slots_per_row = shape->max_pages - a.page_begin;
     a.extra_pieces = E;
-    a.extra_slot0 = rows + grid.total_warps;
+    a.extra_slot0 = rows + full.total_warps;
     a.wait_at_exit = 0;
     a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
@@ -650,6 +657,7 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     p.num_pool_pages = shape->num_pool_pages;
     p.prefix_pages = prefix_pages;
     p.splits = E;
+    p.ctas = pctas;
     p.slot0 = a.extra_slot0;
     p.scale_log2 = a.scale_log2;
 

@@ -42,6 +42,11 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+// Invalidates an mbarrier with no pending arrivals so that it can be initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -405,6 +410,7 @@ struct PrefixArgs {
     int32_t batch, num_q_heads, num_kv_heads, group, page_size, max_pages, num_pool_pages;
     int32_t prefix_pages;   // logical pages [0, prefix_pages) are shared by every row
     int32_t splits;         // key splits per (tile, head)
+    int32_t ctas;           // persistent grid size (<= tiles x heads x splits)
     int64_t slot0;          // row r's split s writes slot slot0 + r * splits + s
     float scale_log2;
 };
@@ -414,6 +420,12 @@ constexpr int kPrefixKeys = 128;      // keys per prefix block (the S tile's N)
 constexpr int kPrefixRowThreads = 2;  // softmax threads per query row (each owns 64 of a block's keys)
 constexpr int kPrefixThreads = 128 * kPrefixRowThreads + 96;  // softmax warps, MMA warp, K and V TMA warps
 constexpr int kMaxPrefixSplits = 64;
+// Share of the SMs the persistent prefix grid of a cascade decode takes; the
+// paged decode of the rows' own pages gets the others.  Measured on GB300 at
+// the shared-prefix workload (128 prefix items): 26 / 32 / 43 / 64 CTAs gave
+// 146 / 127 / 106 / 105 us per step (the prefix items slow to ~30 us each
+// beside the decode's HBM stream, so the prefix needs ~40 % of the SMs).
+constexpr float kPrefixSmShare = 0.43f;
 
 // Warps whose unit ranges intersect row `row` (none when there are no units).
 __device__ __forceinline__ void row_warps(const DecodeArgs &a, int row, int64_t &w0, int64_t &w1) {

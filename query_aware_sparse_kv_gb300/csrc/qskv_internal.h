@@ -62,6 +62,8 @@ cudaError_t launch_merge(const DecodeArgs &a, int head_dim, cudaStream_t stream)
 // head, and the key splits per (tile, head) chosen for a device with
 // `num_sms` SMs (0 when the prefix is empty).
 int prefix_tiles(int batch, int group);
+// Persistent CTAs of the prefix grid for `items` items on a device with `num_sms` SMs.
+int prefix_ctas(int items, int num_sms);
 int prefix_splits(int batch, int group, int num_kv_heads, int page_size, int prefix_pages, int num_sms);
 cudaError_t launch_prefix(const PrefixArgs &a, const CUtensorMap *tmap_k, const CUtensorMap *tmap_v, int q_dtype,
                           int head_dim, cudaStream_t stream);
