@@ -675,11 +675,11 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
     const bool private_pages = a.selected != nullptr || a.page_begin > 0;
     da.kv_evict_first = private_pages && l2 > 0 && kv_bytes > double(l2) ? 1 : 0;
     if (prefix) {
-        // cascade: the shared prefix first; it waits for the previous kernel
-        // and then releases the decode of the rows' own pages, which runs on
-        // the SMs the prefix grid leaves free and, in its place, as prefix
-        // CTAs finish.  The decode waits for the prefix grid only at its
-        // exit, so the merge behind it sees both.
+        // cascade: the shared prefix first, as a persistent grid on a share
+        // of the SMs; it waits for the previous kernel and then releases the
+        // decode of the rows' own pages, whose grid (sized by the caller to
+        // the other SMs) runs beside it.  The decode waits for the prefix
+        // grid only at its exit, so the merge behind it sees both.
         if (kv_dtype != kDtypeBf16) return cudaErrorInvalidValue;
         cudaError_t e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
         if (e != cudaSuccess) return e;

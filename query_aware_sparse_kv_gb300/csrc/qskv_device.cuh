@@ -397,7 +397,8 @@ struct DecodeArgs {
 };
 
 // Shared-prefix cascade: the attention of all B x G query rows of one KV head
-// over the shared prefix, one CTA per (128-row tile, KV head, key split).
+// over the shared prefix, in work items of (128-row tile, KV head, key split)
+// taken by a persistent grid of `ctas` CTAs.
 struct PrefixArgs {
     const void *q;          // [B][Hq][D]
     const void *k_pool;     // [Npool][Hkv][P][D] bf16 (for L2 prefetch; loads go through the tensor maps)
