@@ -88,6 +88,18 @@ def test_long_prefix_many_splits(oracle_lib):
     _check(inp, _cascade(inp), oracle_lib)
 
 
+def test_persistent_prefix_grid_all_rows(oracle_lib):
+    """The prefix grid is persistent (about 43 % of the SMs): at 64 sequences,
+    8 KV heads and a 64-page prefix there are 128 work items, so each prefix
+    CTA takes two of them in turn (mbarriers re-armed in between) while the
+    paged decode runs on the other SMs.  Every row is checked."""
+    spec = W.Spec(name="cascade", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                  top_k=None, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, kind="shared_prefix",
+                  prefix_pages=64, suffix_pages=4, seq_lens=_ragged(64, 64, 4, 16, seed=5), seed=24)
+    inp = W.make_inputs(spec)
+    _check(inp, _cascade(inp), oracle_lib)
+
+
 def test_prefix_is_the_whole_sequence(oracle_lib):
     # no private pages at all: max_pages == prefix_pages, the paged decode has no work
     spec = _spec(batch=4, prefix=6, suffix=0, seq=(96,) * 4, seed=22)
