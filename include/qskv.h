@@ -58,7 +58,9 @@
  * Query head h reads KV head h / G, G = num_q_heads / num_kv_heads.
  *
  * Supported: head_dim 64 or 128; page_size 16 or 32; G in {1, 2, 4, 8};
- * kv dtype fp32 or bf16 (meta has the kv dtype); q dtype fp32 or bf16.
+ * kv dtype fp32 or bf16 (meta has the kv dtype); q dtype fp32 or bf16;
+ * batch * num_kv_heads <= 65535 (every call returns QSKV_ERR_UNSUPPORTED
+ * beyond).
  * Every device pointer that is read or written in 16-byte vectors (q, k_pool,
  * v_pool, meta, out) must be 16-byte aligned; int32 arrays 4-byte aligned.
  *
