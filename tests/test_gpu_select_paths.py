@@ -5,8 +5,10 @@ overview item 3: the lossy variant).
 The selected list must equal, index for index, the oracle's rule applied to
 the GPU's own fp32 scores: the exact top-K with ties to the lower page index,
 or the lossy top-K.  Cases cover clustered bound scores, heavy ties, rows
-shorter than K, and rows longer than the 4096 keys the kernel keeps in
-shared memory (those read their keys from global memory in every pass).
+shorter than K, rows of 2048 to 4096 pages (compacted by per-thread runs
+rather than warp ballots) and rows longer than the 4096 keys the kernel
+keeps in shared memory (those read their keys from global memory in every
+pass).
 Each batch is ranked twice, with its own page table and with the table
 padded by -1 columns: width must change nothing."""
 import numpy as np
@@ -45,6 +47,8 @@ CASES = {
                                              top_k=128)),
     "ties": lambda: _ties(W.Spec(name="ties", batch=3, num_q_heads=4, num_kv_heads=2, head_dim=64, page_size=16,
                                  seq_lens=(16 * 2000, 16 * 700 + 5, 16 * 40), top_k=100, kind="iid", seed=41)),
+    "long_rows": lambda: W.make_inputs(W.spec_for("long_context", batch=2, seq_len_range=(70000, 130000),
+                                                  max_pages=None, top_k=128)),
     "beyond_smem": lambda: W.make_inputs(W.Spec(name="long_rows", batch=2, num_q_heads=8, num_kv_heads=2,
                                                 head_dim=64, page_size=16, seq_lens=(16 * 4500 + 3, 16 * 4200),
                                                 top_k=200, kind="iid", seed=43)),
