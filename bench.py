@@ -481,8 +481,8 @@ def run_gpu(args):
     # captured by PagedDecoder.capture_step with the host buffers: its
     # kernels read the step's query from pinned host memory and write the
     # output into pinned host memory (zero-copy over the host link); the host
-    # waits for it before the next step (a serving loop needs the output to
-    # go on).
+    # waits for it (PagedDecoder.wait, an event poll) before the next step (a
+    # serving loop needs the output to go on).
     e2e_steps = 0 if args.no_e2e else min(args.steps, 500)
     q_host = qv_cpu.pin_memory()
     q_dev = torch.empty_like(qv[0])
@@ -498,7 +498,7 @@ def run_gpu(args):
         t0 = time.perf_counter()
         for i in range(e2e_steps):
             graphs[i % N_Q_VARIANTS]()
-            torch.cuda.current_stream().synchronize()
+            dec.wait()
         s = max_over_ranks(time.perf_counter() - t0, world, dev)
         dec.check()
         return world * e2e_steps / s
@@ -538,7 +538,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "step_launch": "CUDA graph replay, one graph per query variant (meta refresh + selection + decode)",
         "eager_ms_per_step": eager_ms,
-        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to pinned host memory (zero-copy), host sync per step", "copy_nodes_value": e2e_copy_nodes,
+        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)", "copy_nodes_value": e2e_copy_nodes,
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
         # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking;

@@ -147,6 +147,20 @@ class PagedDecoder:
             body()
         return graph.replay
 
+    def wait(self, stream=None):
+        """Block the host until all work issued so far on ``stream`` (the
+        current stream by default) has run, by polling an event recorded
+        behind it (a busy wait on the host), which returns slightly sooner
+        than a stream synchronisation; for serving loops that wait for every
+        step's output."""
+        st = torch.cuda.current_stream() if stream is None else stream
+        ev = getattr(self, "_wait_event", None)
+        if ev is None:
+            ev = self._wait_event = torch.cuda.Event()
+        ev.record(st)
+        while not ev.query():
+            pass
+
     def check(self, stream=None):
         """Raise if the device flagged an out-of-range index or a timeout."""
         st = B.get_error(self.workspace, stream)

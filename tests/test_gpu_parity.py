@@ -276,7 +276,7 @@ def test_zero_copy_step_matches_the_device_path(oracle_lib, case):
     for v in (0, 1, 0):
         out_host.zero_()
         graphs[v]()
-        torch.cuda.current_stream().synchronize()
+        dec.wait()  # event poll: returns only once the output is in host memory
         assert torch.equal(out_host, want[v])
     dec.check()
 
