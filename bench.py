@@ -312,7 +312,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / steps_per_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, args.scorer, args.approx_eps),
+        "config": workload_config(spec, args.scorer, args.approx_eps, inputs),
         "cpu_baseline": {"value": steps_per_s, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": steps_per_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -321,7 +321,31 @@ def run_reference(args):
     return 0
 
 
-def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None) -> dict:
+L2_BYTES = 129e6  # GB300 L2
+
+
+def l2_note(inputs: dict) -> str:
+    """How the timed steps relate to L2: the KV pool's size and one step's
+    selected (or, dense, every) K/V bytes against the 129 MB L2."""
+    spec = inputs["spec"]
+    pool = 2 * inputs["k_pool"].numel() * inputs["k_pool"].element_size()
+    P, d, Hkv = spec.page_size, spec.head_dim, spec.num_kv_heads
+    page = 2 * P * d * inputs["k_pool"].element_size()
+    nb = inputs["n_pages"].long()
+    pages = (torch.clamp(nb, max=spec.top_k) if spec.top_k is not None else nb).sum().item() * Hkv
+    if spec.kind == "shared_prefix" and spec.top_k is None:
+        pages = (nb.sum().item() - (spec.batch - 1) * spec.prefix_pages) * Hkv  # unique pages
+    step = pages * page
+    if pool <= L2_BYTES:
+        return f"inputs fit in L2 (KV pool {pool / 1e6:.1f} MB; correctness workload), no flush"
+    if step > L2_BYTES:
+        return (f"KV pool {pool / 1e9:.2f} GB and one step's K/V {step / 1e6:.0f} MB both exceed L2; "
+                f"16 rotating query variants")
+    return (f"KV pool {pool / 1e9:.2f} GB exceeds L2; one step's K/V ({step / 1e6:.0f} MB) fits in L2 and "
+            f"partly repeats across the 16 rotating query variants, as consecutive decode steps do; no flush")
+
+
+def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None, inputs=None) -> dict:
     desc = {
         "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
         "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
@@ -339,7 +363,7 @@ def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None) -> dic
             (list(spec.seq_lens)[:1] if spec.seq_lens else None),
             "top_k": spec.top_k, "kv_dtype": str(spec.kv_dtype).replace("torch.", ""),
             "q_dtype": str(spec.q_dtype).replace("torch.", ""),
-            "l2": "inputs larger than L2 (KV pool and metadata) + 16 rotating query variants"}
+            "l2": l2_note(inputs) if inputs is not None else "KV pool larger than L2, 16 rotating query variants"}
 
 
 # ------------------------------------------------------------------ main --
@@ -525,7 +549,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": workload_config(spec, args.scorer, args.approx_eps),
+        "config": workload_config(spec, args.scorer, args.approx_eps, inputs),
         "effective_gbs": step_gbs,
         "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
         "bytes_per_step": nbytes,

@@ -48,3 +48,30 @@ def test_cascade_counts_the_prefix_once():
     inp = W.make_inputs(spec)
     nb = bench.step_bytes(inp, None, None, prefix_pages=2)
     assert nb["kv"] == 8 * (2 + 3 * 1) * 16 * 128 * 2 * 2
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` runs the oracle on the host cores (no GPU)
+    and prints the contract's JSON line for the reference arm."""
+    import json
+    import subprocess
+    import sys
+
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=str(__import__("pathlib").Path(bench.__file__).parent))
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["l2"].startswith("inputs fit in L2")
+
+
+def test_l2_note_states_what_holds():
+    llama = W.make_inputs(W.spec_for("llama3_8b", batch=2, seq_len_range=(30000, 32000)))
+    assert "both exceed L2" not in bench.l2_note(llama)  # 2 x 8 rows x 128 pages x 8 KB = 17 MB a step
+    assert "exceeds L2" in bench.l2_note(llama)
