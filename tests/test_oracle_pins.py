@@ -274,6 +274,32 @@ def test_lse_merge_of_two_page_sets_equals_the_union(oracle_lib):
     np.testing.assert_allclose(lse, lu, rtol=1e-13)
 
 
+@pytest.mark.parametrize("splits", [1, 2, 7])
+def test_lse_merge_is_independent_of_the_split_count(oracle_lib, splits):
+    """The split-K decode's merge: the row's pages cut into `splits`
+    contiguous ranges (some ending inside the partial last page's range),
+    each attended alone, then folded by log-sum-exp one piece at a time with
+    a running maximum (the order the merge kernel uses), give attention over
+    all pages: the result does not depend on the split count."""
+    inp = _small(kv=torch.bfloat16, seq_lens=(61,), hq=4, hkv=1, d=16, P=8)
+    pages = list(range(8))  # 61 tokens in 8-token pages: the last page holds 5
+    cuts = np.linspace(0, len(pages), splits + 1).round().astype(int)
+    pieces = [oracle_lib.attend_row(inp, 0, 0, pages[cuts[i]:cuts[i + 1]]) for i in range(splits)]
+    mx = np.full(4, -np.inf)
+    den = np.zeros(4)
+    acc = np.zeros((4, 16))
+    for o, lse in pieces:
+        m = np.maximum(mx, lse)
+        scale = np.exp(mx - m)
+        w = np.exp(lse - m)
+        den = den * scale + w
+        acc = acc * scale[:, None] + w[:, None] * o
+        mx = m
+    ou, lu = oracle_lib.attend_row(inp, 0, 0, pages)
+    np.testing.assert_allclose(acc / den[:, None], ou, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(mx + np.log(den), lu, rtol=1e-13)
+
+
 def test_physical_layout_does_not_matter(oracle_lib):
     """PagedAttention (CS336 s9.2): moving pages to other physical slots and
     rewriting the table leaves the result unchanged."""
