@@ -456,17 +456,25 @@ def run_gpu(args):
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev) if args.flush_l2 else None
+    step_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if args.flush_l2 else None)
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
+        if flush is not None:  # L2 emptied before the step; the write is outside the step's events
+            flush.fill_(float(i))
+            step_ev[i][0].record(stream)
         step_graphs[i % N_Q_VARIANTS].replay()
+        if flush is not None:
+            step_ev[i][1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     barrier(world)
-    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = (sum(a.elapsed_time(b) for a, b in step_ev) if flush is not None else start.elapsed_time(stop))
     clocks = None
     if sampler:
         time.sleep(0.25)
@@ -549,7 +557,9 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": workload_config(spec, args.scorer, args.approx_eps, inputs),
+        "config": dict(workload_config(spec, args.scorer, args.approx_eps, inputs),
+                       **({"l2": "L2 flushed (2 x 129 MB write) before every timed step; each step timed by its own events"}
+                          if args.flush_l2 else {})),
         "effective_gbs": step_gbs,
         "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
         "bytes_per_step": nbytes,
@@ -594,6 +604,8 @@ def main(argv=None):
     ap.add_argument("--approx-eps", type=float, default=None,
                     help="lossy top-K: stop once floor(eps * K) pages are undecided and sample them")
     ap.add_argument("--seed", type=int, default=0, help="seed of the lossy top-K's sampling")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write 2 x L2 before every timed step and time each step by its own events (cold L2)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)
