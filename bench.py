@@ -61,7 +61,9 @@ def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray
             dtype for the bound scorer, d fp32 for the centroid scorer), q,
             one page-table entry per page, the fp32 score written and read
             back, the selected list written;
-    meta:   the valid key rows of each sequence's last page, its metadata written.
+    meta:   the valid key rows of each sequence's last page, its metadata
+            written (sparse decode only: a dense decode reads no metadata,
+            so its step has no refresh).
     """
     spec = inputs["spec"]
     B, Hq, Hkv, d, P = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
@@ -96,7 +98,7 @@ def step_bytes(inputs: dict, selected: np.ndarray | None, n_selected: np.ndarray
         total_pages = int(nb.sum()) * Hkv
         select = total_pages * (meta_row + 4 + 8) + q_bytes + sel_bytes
     last_valid = seq - (nb - 1) * P
-    meta = int(sum(int(v) * d * s + meta_row for v in last_valid)) * Hkv
+    meta = 0 if top_k is None else int(sum(int(v) * d * s + meta_row for v in last_valid)) * Hkv
     return dict(decode=decode, select=select, meta=meta, total=decode + select + meta, kv=kv)
 
 
@@ -414,8 +416,8 @@ def run_gpu(args):
     nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
 
     def select_part(v):
-        dec.build_meta(last_ids, last_valid)
-        if spec.top_k is not None:
+        if spec.top_k is not None:  # a dense decode reads no metadata: no refresh
+            dec.build_meta(last_ids, last_valid)
             dec.select(q=qv[v])
 
     def decode_part(v):
@@ -521,7 +523,8 @@ def run_gpu(args):
     q_dev.copy_(qv[0])
     out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
     def e2e_run(zero_copy):
-        graphs = [dec.capture_step(q_dev, last_ids, last_valid, q_host=q_host[v], out_host=out_host,
+        refresh = (last_ids, last_valid) if spec.top_k is not None else (None, None)
+        graphs = [dec.capture_step(q_dev, *refresh, q_host=q_host[v], out_host=out_host,
                                    zero_copy=zero_copy) for v in range(N_Q_VARIANTS)]
         for i in range(min(e2e_steps, args.warmup)):
             graphs[i % N_Q_VARIANTS]()
@@ -570,14 +573,16 @@ def run_gpu(args):
                      "decode_ms": decode_ms, "bytes_per_launch": nbytes["decode"],
                      "traffic": ncu_traffic(args.workload)},
         "cpu_baseline": cpu,
-        "step_launch": "CUDA graph replay, one graph per query variant (meta refresh + selection + decode)",
+        "step_launch": ("CUDA graph replay, one graph per query variant (meta refresh + selection + decode)"
+                        if spec.top_k is not None else
+                        "CUDA graph replay, one graph per query variant (dense decode: no metadata refresh or selection)"),
         "eager_ms_per_step": eager_ms,
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)", "copy_nodes_value": e2e_copy_nodes,
                 "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
-        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: no scoring/ranking;
-        # cascade: + the shared-prefix kernel)
-        "gpu_launches": (5 if spec.top_k is not None else (4 if prefix else 3)) * args.steps,
+        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: decode and
+        # merge only; cascade: + the shared-prefix kernel)
+        "gpu_launches": (5 if spec.top_k is not None else (3 if prefix else 2)) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
