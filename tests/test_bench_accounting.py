@@ -38,6 +38,7 @@ def test_dense_counts_every_page():
     inp = W.make_inputs(spec)
     nb = bench.step_bytes(inp, None, None)
     assert nb["kv"] == 3 * 8 * 3 * 16 * 128 * 2 * 2
+    assert nb["meta"] == 0 and nb["select"] == 0  # a dense step reads no metadata
     assert nb["select"] == 0
 
 
