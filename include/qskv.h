@@ -201,20 +201,24 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
  * reports recall@k > 0.97 at 1.3-1.6x the exact kernel's speed).
  * Scores as qskv_page_select (scorer QSKV_SCORE_BOUND: meta = [m | M] rows in
  * meta_dtype) or qskv_page_select_centroid (QSKV_SCORE_CENTROID: meta = fp32
- * centroids, meta_dtype QSKV_F32).  Ranking: the exact MSB-first radix passes
- * over 8-bit digits of the order-preserving score keys run until at most
- * floor(epsilon * top_k) keys are undecided; every key above the threshold
- * digit bucket is kept, and the `need` still missing are drawn from that
- * bucket's m keys (ranked t = 0..m-1 in page order) by systematic sampling:
- * key t is kept iff floor(((t+1) need + o) / m) - floor((t need + o) / m) = 1,
- * with o = SplitMix64 output (row + 1) from `seed` (Steele, Lea and Flood
- * 2014), mod m.  Hence recall@top_k >= 1 - epsilon against the exact top-K
- * of the same fp32 scores, exactly min(top_k, n_b) pages, ascending.
- * epsilon in [0, 1); 0 gives exactly qskv_page_select's result.
+ * centroids, meta_dtype QSKV_F32).  Ranking: the fp32 scores become
+ * order-preserving 32-bit keys, and exact MSB-first radix passes over the
+ * key's four 8-bit digits (bits 31..24, 23..16, 15..8, 7..0) narrow down
+ * the threshold digit bucket until at most need_max keys are undecided,
+ *   need_max = floor(epsilon * top_k)   (one IEEE double multiplication),
+ * checked before each pass; every key above the threshold bucket is kept,
+ * and the `need` still missing are drawn from that bucket's m keys (ranked
+ * t = 0..m-1 in page order) by systematic sampling: key t is kept iff
+ * floor(((t+1) need + o) / m) - floor((t need + o) / m) = 1, with
+ * o = SplitMix64 output (row + 1) from `seed` (Steele, Lea and Flood 2014),
+ * mod m.  Hence recall@top_k >= 1 - epsilon against the exact top-K of the
+ * same fp32 scores, exactly min(top_k, n_b) pages, ascending.
+ * epsilon in [0, 1); need_max = 0 (e.g. epsilon = 0) gives exactly
+ * qskv_page_select's result.
  */
 qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtype q_dtype, const void *meta,
                                     qskv_dtype meta_dtype, const int32_t *page_table, const int32_t *seq_lens,
-                                    const qskv_shape *shape, int32_t top_k, float epsilon, uint64_t seed,
+                                    const qskv_shape *shape, int32_t top_k, double epsilon, uint64_t seed,
                                     int32_t *selected, int32_t *n_selected, float *scores, void *workspace,
                                     size_t workspace_bytes, void *stream);
 

@@ -199,15 +199,17 @@ def splitmix64(seed: int, i: int) -> int:
 
 
 def need_max(top_k: int, epsilon: float) -> int:
-    """Early-exit threshold of the approximate top-K: floor(epsilon * K)."""
-    return int(math.floor(epsilon * top_k))
+    """Early-exit threshold of the approximate top-K: floor(epsilon * K), the
+    product taken as one IEEE double multiplication (epsilon is a double)."""
+    return int(math.floor(float(epsilon) * float(top_k)))
 
 
 def select_approx(scores_f32, top_k: int, epsilon: float, seed: int, row: int) -> tuple[np.ndarray, int]:
     """Vortex item 3: lossy radix top-K over fp32 scores -- exact radix passes
-    until at most floor(epsilon * K) keys are undecided, then those drawn by
-    systematic random sampling from the threshold bin.  epsilon = 0 is the
-    exact rule.  Returns (ascending indices, -1 padded to top_k; count)."""
+    over the key's four 8-bit digits (most significant first) until at most
+    floor(epsilon * K) keys are undecided, then those drawn by systematic
+    random sampling from the threshold bin.  epsilon = 0 is the exact rule.
+    Returns (ascending indices, -1 padded to top_k; count)."""
     s = np.ascontiguousarray(scores_f32, dtype=np.float32)
     sel = np.empty(max(top_k, 1), dtype=np.int32)
     n = _load().orc_select_approx(s.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), len(s), top_k,

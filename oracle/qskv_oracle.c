@@ -340,11 +340,11 @@ static uint32_t key_of(float f) {
  * [VXR] Approximate top-K of one row of fp32 scores (the reading taken for
  * the digest's lossy radix Top-K):
  *   1. scores become order-preserving 32-bit keys;
- *   2. MSB-first radix passes over 8-bit digits, starting at the highest bit
- *      where the row's keys differ: each pass counts the keys of the current
- *      bucket per digit and moves into the digit bucket that holds the
- *      `need`-th largest key; keys in higher digit buckets are certain to be
- *      in the top-K and leave `need`;
+ *   2. MSB-first radix passes over the four 8-bit digits of the key (bits
+ *      31..24, then 23..16, 15..8, 7..0): each pass counts the keys of the
+ *      current bucket per digit and moves into the digit bucket that holds
+ *      the `need`-th largest key; keys in higher digit buckets are certain
+ *      to be in the top-K and leave `need`;
  *   3. early exit: before a pass, if need <= need_max (= floor(eps * K)),
  *      stop; also stop when the bucket is taken whole or fully resolved;
  *   4. the keys above the final bucket are all kept; `need` keys of the
@@ -364,16 +364,10 @@ int orc_select_approx(const float *scores, int n, int top_k, int need_max, uint6
         return n;
     }
     uint32_t *key = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int i = 0; i < n; i++) {
-        key[i] = key_of(scores[i]);
-        if (key[i] < kmin) kmin = key[i];
-        if (key[i] > kmax) kmax = key[i];
-    }
-    uint32_t diff = kmin ^ kmax;
-    int hi = 0;
-    while (hi < 32 && (diff >> hi) != 0u) hi++; /* bits >= hi are common to all keys */
-    uint64_t prefix = hi >= 32 ? 0u : ((uint64_t)kmax >> hi) << hi;
+    for (int i = 0; i < n; i++) key[i] = key_of(scores[i]);
+    /* the bucket is the keys whose bits >= hi equal those of `prefix` */
+    int hi = 32;
+    uint64_t prefix = 0;
     int need = top_k, lo = hi;
     while (hi > 0) {
         if (need_max > 0 && need <= need_max) break;

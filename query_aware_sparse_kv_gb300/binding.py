@@ -74,7 +74,7 @@ def load(path: str = LIB_PATH):
                                               sz, vp]
     lib.qskv_page_select_approx.restype = ctypes.c_int
     lib.qskv_page_select_approx.argtypes = [ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int, i32p, i32p, sp, i32,
-                                            ctypes.c_float, ctypes.c_uint64, i32p, i32p, f32p, vp, sz, vp]
+                                            ctypes.c_double, ctypes.c_uint64, i32p, i32p, f32p, vp, sz, vp]
     lib.qskv_sparse_paged_decode.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p, i32p, i32,
                                              ctypes.c_float, f32p, f32p, vp, sz, vp]

@@ -605,12 +605,16 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     const size_t smem = decode_smem_bytes(D, a.stages);
     auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
+    static std::mutex mu;                // calls may come from several host threads
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || configured[dev] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = smem;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || configured[dev] < smem) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = smem;
+        }
     }
     return launch_pdl(kernel, dim3(grid.ctas), dim3(WPC * 32), smem, stream, *tk, *tv, a);
 }

@@ -202,9 +202,15 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
         kmax = max(kmax, s_mm[NT / 32 + w]);
     }
 
-    // Bits at and above `hi` are shared by every key of the row.
+    // Bits at and above `hi` are shared by every key of the row: the passes
+    // over digits above them would find one bucket holding every key and
+    // decide nothing.  The exact select starts its 8-bit digits right below
+    // them (the first pass then splits the row); the lossy select keeps the
+    // key's fixed digits (bits 31..24, 23..16, ...), on which its early exit
+    // is defined, and only skips the digits shared by every key.
     const uint32_t diff = kmin ^ kmax;
     int hi = diff ? 32 - __clz(diff) : 0;
+    if (a.need_max > 0) hi = (hi + 7) & ~7;
     uint32_t prefix = hi >= 32 ? 0u : (kmax & ~((1u << hi) - 1u));
     int need = K;  // keys still to take among those matching `prefix` above `hi`
     int lo = hi;

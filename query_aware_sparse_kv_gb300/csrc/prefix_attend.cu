@@ -48,6 +48,8 @@
 // bounded; a wait that gives up flags a timeout, stops the CTA's other
 // roles, lets issued copies and MMAs complete and frees the tensor memory
 // before the CTA exits.
+#include <mutex>
+
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
 
@@ -543,12 +545,16 @@ cudaError_t launch_prefix_t(const PrefixArgs &a, const CUtensorMap *tk, const CU
     using C = PrefixCfg<D, QF32>;
     auto kernel = prefix_attend_kernel<D, QF32>;
     static bool configured[64] = {false};  // dynamic smem limit set, per device
+    static std::mutex mu;                  // calls may come from several host threads
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || !configured[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = true;
+        }
     }
     return launch_pdl(kernel, dim3(ctas), dim3(kPrefixThreads), size_t(C::SMEM), stream, *tk, *tv, a);
 }

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -42,13 +43,16 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
 }
 
 int l2_cache_bytes() {
-    static int cache[128] = {0};
+    static std::atomic<int> cache[128];  // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 128) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 128) cache[dev] = n;
+    if (dev >= 0 && dev < 128) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -79,14 +83,17 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // SM count of the current device (cached per device).
 int current_sm_count(int *device_out) {
-    static int cache[128] = {0};
+    static std::atomic<int> cache[128];  // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (device_out) *device_out = dev;
-    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    if (dev >= 0 && dev < 128) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 128) cache[dev] = n;
+    if (dev >= 0 && dev < 128) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -344,7 +351,7 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
 
 qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtype q_dtype, const void *meta,
                                     qskv_dtype meta_dtype, const int32_t *page_table, const int32_t *seq_lens,
-                                    const qskv_shape *shape, int32_t top_k, float epsilon, uint64_t seed,
+                                    const qskv_shape *shape, int32_t top_k, double epsilon, uint64_t seed,
                                     int32_t *selected, int32_t *n_selected, float *scores, void *workspace,
                                     size_t workspace_bytes, void *stream) {
     QSKV_TRY(check_shape(shape));
@@ -354,7 +361,7 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
         return fail(QSKV_ERR_INVALID_ARG, "unknown scorer %d", int(scorer));
     if (scorer == QSKV_SCORE_CENTROID && meta_dtype != QSKV_F32)
         return fail(QSKV_ERR_INVALID_ARG, "centroid metadata is fp32");
-    if (!(epsilon >= 0.f && epsilon < 1.f)) return fail(QSKV_ERR_INVALID_ARG, "epsilon must be in [0, 1)");
+    if (!(epsilon >= 0.0 && epsilon < 1.0)) return fail(QSKV_ERR_INVALID_ARG, "epsilon must be in [0, 1)");
     if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
     if (!q || !meta || !page_table || !seq_lens || !selected || !n_selected)
         return fail(QSKV_ERR_INVALID_ARG, "q, meta, page_table, seq_lens, selected and n_selected must be non-NULL");
@@ -386,7 +393,7 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
     a.max_pages = shape->max_pages;
     a.num_pool_pages = shape->num_pool_pages;
     a.top_k = top_k;
-    a.need_max = int32_t(floor(double(epsilon) * double(top_k)));
+    a.need_max = int32_t(floor(epsilon * double(top_k)));
     a.seed = seed;
     a.meta_evict_first = 0;
     a.head_quads = 0;

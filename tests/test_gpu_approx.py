@@ -1,12 +1,16 @@
 """GPU parity of the lossy top-K (Vortex digest, method overview item 3:
 radix Top-K with early exit and random sampling from the threshold bin).
 
-The approximate selection is a function of the fp32 scores, so the GPU's
-selected list must equal, index for index, the oracle's approximate rule
-run on the GPU's own fp32 scores (the integer decisions are taken in the
-same precision on both sides; the random start is SplitMix64 on both).  On
-top: recall@K >= 1 - epsilon against the exact top-K, epsilon = 0 equal to
-the exact call, and outputs against oracle attention over the pages kept."""
+The GPU's fp32 scores are first checked against the oracle's fp64 scores
+(the bound within the fp32 summation tolerance, the centroid score within
+its derived error bound).  The approximate selection is a function of the
+fp32 scores, so the GPU's selected list must then equal, index for index,
+the oracle's approximate rule run on the GPU's own fp32 scores (the integer
+decisions are taken in the same precision on both sides; the early-exit
+threshold floor(epsilon * K) is one double multiplication on both; the
+random start is SplitMix64 on both).  On top: recall@K >= 1 - epsilon
+against the exact top-K, epsilon = 0 equal to the exact call, and outputs
+against oracle attention over the pages kept."""
 import numpy as np
 import pytest
 import torch
@@ -38,6 +42,11 @@ def _run(inputs, oracle, eps, seed, scorer="bound", rows=None):
     dec = qskv.from_inputs(inputs, scorer=scorer, approx_epsilon=eps, approx_seed=seed)
     ids, vt = oracle.all_pages(inputs)
     dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    if scorer == "centroid":
+        o_meta = oracle.centroids(inputs["k_pool"], ids, vt)
+        cent_tol = PR.centroid_tolerance(inputs["k_pool"], ids, vt)
+    else:
+        o_meta = oracle.meta(inputs["k_pool"], ids, vt)
     sc = torch.full(tuple(dec.selected.shape[:2]) + (inputs["page_table"].shape[1],), float("nan"), device="cuda")
     dec.select(scores=sc)
     dec.decode()
@@ -53,10 +62,21 @@ def _run(inputs, oracle, eps, seed, scorer="bound", rows=None):
     tol = PR.out_tolerance(spec.kv_dtype)
     n_rows = spec.batch * Hkv
     worst_recall = 1.0
+    q = inputs["q"].double().numpy()
     for r in (range(n_rows) if rows is None else rows):
         b, g = divmod(int(r), Hkv)
         n_b = PR.n_pages_of(inputs, b)
         s = scores[b, g, :n_b]
+        # the GPU's scores against the oracle's, before they decide anything
+        qg = q[b, g * G:(g + 1) * G]
+        if scorer == "centroid":
+            o_scores = oracle.centroid_row_scores(qg, o_meta, inputs["page_table"][b], n_b, g)
+            stol = PR.centroid_score_tolerance(qg, o_meta, cent_tol, inputs["page_table"][b], n_b, g)
+            err = np.abs(s.astype(np.float64) - o_scores)
+            assert (err <= stol).all(), f"row {r}: centroid score error {err.max()}"
+        else:
+            PR.assert_scores_close(s, oracle.row_scores(qg, o_meta, inputs["page_table"][b], n_b, g), n_b,
+                                   f"row {r}")
         want, cnt = oracle.select_approx(s, K, eps, seed, r)
         assert nsel[b, g] == cnt and sel[b, g].tolist() == want.tolist(), f"row {r}: selection differs"
         if K < n_b:
@@ -73,6 +93,18 @@ def _run(inputs, oracle, eps, seed, scorer="bound", rows=None):
 @pytest.mark.parametrize("eps", [0.03, 0.1])
 def test_approx_selection_matches_the_oracle_rule(oracle_lib, name, eps):
     _run(W.make_inputs(SMALL[name]), oracle_lib, eps, seed=1234 + int(eps * 100))
+
+
+@pytest.mark.parametrize("eps,top_k", [(0.03, 100), (0.01, 100), (0.7, 10), (0.57, 100)])
+def test_approx_threshold_pairs_where_float_rounding_differs(oracle_lib, eps, top_k):
+    """(epsilon, K) pairs whose need_max = floor(epsilon * K) depends on the
+    precision it is computed in (a single-precision epsilon gives 2, 0, 6 and
+    56 against 3, 1, 7 and 56 in double): the library and the oracle both
+    take the double product, so their selections agree index for index."""
+    spec = W.spec_for("llama3_8b", batch=3, seq_len_range=(2000, 6000), max_pages=None, top_k=top_k)
+    assert oracle_lib.need_max(top_k, eps) == {(0.03, 100): 3, (0.01, 100): 1, (0.7, 10): 7,
+                                                (0.57, 100): 56}[(eps, top_k)]
+    _run(W.make_inputs(spec), oracle_lib, eps, seed=2024)
 
 
 def test_approx_with_the_centroid_scorer(oracle_lib):

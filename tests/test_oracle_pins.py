@@ -582,7 +582,7 @@ def test_approx_sampling_is_uniform_over_the_threshold_bin(oracle_lib):
     s = np.zeros(n, dtype=np.float32)
     s[:60] = 5.0  # 60 certain keys; the other 940 tie in the threshold bin
     need, m = k - 60, n - 60
-    eps = need / k  # need_max = 40: stop before the first pass
+    eps = need / k  # need_max = 40: stop after the first pass (top digit)
     hits = np.zeros(n)
     trials = 3000
     for seed in range(trials):
@@ -605,3 +605,38 @@ def test_approx_select_is_deterministic_per_seed_and_row(oracle_lib):
     d, _ = oracle_lib.select_approx(s, 200, 0.2, 42, 10)
     assert a.tolist() == b.tolist()
     assert a.tolist() != c.tolist() and a.tolist() != d.tolist()
+
+
+def test_approx_need_max_is_the_double_product_floored(oracle_lib):
+    """need_max = floor(epsilon * K) with epsilon and the product in IEEE
+    double: 0.03 * 100 and 0.7 * 10 round to the integers 3 and 7, 0.57 * 100
+    to 56.99999999999999 (so 56), and a single-precision epsilon would give
+    2, 0 and 6 for the first three."""
+    assert oracle_lib.need_max(100, 0.03) == 3
+    assert oracle_lib.need_max(100, 0.01) == 1
+    assert oracle_lib.need_max(10, 0.7) == 7
+    assert oracle_lib.need_max(100, 0.57) == 56
+    assert oracle_lib.need_max(128, 0.0) == 0
+    f32 = lambda e, k: math.floor(float(np.float32(e)) * k)
+    assert (f32(0.03, 100), f32(0.01, 100), f32(0.7, 10)) == (2, 0, 6)
+
+
+def test_approx_digits_are_the_fixed_bytes_of_the_key(oracle_lib):
+    """The radix digits are the key's fixed bytes (bits 31..24, 23..16, ...).
+    Scores 1 + m/128 + r*2^-16 in [1, 2) share their top byte; their second
+    byte is 0x80 + m.  Three keys sit in a higher second-byte bucket, five in
+    bucket m = 10 whose lower bits differ; with K = 4 and need_max = 1 the
+    select stops after the second byte, so the one missing key is drawn from
+    all five (a start at the highest differing bit would split them by bit
+    15 and draw from two only)."""
+    high = [1 + 90 / 128, 1 + 91 / 128, 1 + 92 / 128]
+    bucket = [1 + 10 / 128 + r * 2.0 ** -16 for r in (1, 2, 3, 257, 258)]
+    s = np.array(high + bucket + [1.0, 1.01], dtype=np.float32)
+    seen = set()
+    for seed in range(400):
+        sel, cnt = oracle_lib.select_approx(s, 4, 0.25, seed, 0)
+        assert cnt == 4 and set(sel[:4].tolist()) >= {0, 1, 2}
+        (extra,) = set(sel[:4].tolist()) - {0, 1, 2}
+        assert 3 <= extra <= 7
+        seen.add(extra)
+    assert seen == {3, 4, 5, 6, 7}

@@ -5,7 +5,9 @@ whose memory planner hands out all of HBM up front and forbids further
 cudaMalloc calls, or latency-critical loops where the allocator (which may
 synchronise the device) must not be called.  qskv_sparse_paged_decode_noalloc
 serves them: it takes the same inputs and outputs as qskv_sparse_paged_decode
-but keeps its scratch in a fixed 8 MiB array built into the library.
+but keeps its scratch in a fixed 8 MiB array built into the library.  Its
+output is checked against the workspace entry point and, row by row, against
+the CPU oracle.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes when run alone.
@@ -45,8 +47,24 @@ def _noalloc(dec, out, lse, dense=False):
     assert st == 0, binding.last_error_message()
 
 
+def _check_against_oracle(inp, dec, out, lse, dense, oracle):
+    """Every row of the entry point's output against the oracle's attention
+    over the same pages (the selection when sparse, every page when dense)."""
+    spec = inp["spec"]
+    Hkv, G = spec.num_kv_heads, spec.group
+    tol = PR.out_tolerance(spec.kv_dtype)
+    o, l = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    sel, nsel = dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy()
+    for r in range(spec.batch * Hkv):
+        b, g = divmod(r, Hkv)
+        n_b = PR.n_pages_of(inp, b)
+        pages = list(range(n_b)) if dense else sel[b, g, :int(nsel[b, g])].tolist()
+        o_out, o_lse = oracle.attend_row(inp, b, g, pages)
+        PR.assert_output_close(o[b, g * G:(g + 1) * G], l[b, g * G:(g + 1) * G], o_out, o_lse, tol, f"row {r}")
+
+
 @pytest.mark.parametrize("name,dense", [("llama", False), ("llama", True), ("tiny", False)])
-def test_noalloc_matches_the_workspace_entry_point_twice(name, dense):
+def test_noalloc_matches_the_workspace_entry_point_twice(oracle_lib, name, dense):
     spec = (W.spec_for("llama3_8b", batch=4, seq_len_range=(900, 3000), max_pages=None, top_k=32)
             if name == "llama" else W.spec_for("tiny"))
     inp = W.make_inputs(spec)
@@ -69,6 +87,7 @@ def test_noalloc_matches_the_workspace_entry_point_twice(name, dense):
         assert torch.isfinite(out).all()
         assert (out - ref_out).abs().max().item() <= tol
         assert (lse - ref_lse).abs().max().item() <= tol
+        _check_against_oracle(inp, dec, out, lse, dense, oracle_lib)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
