@@ -3,9 +3,14 @@
 A step is one pass of the whole hot path over one batch: refresh the
 metadata of the page each sequence appends to, select the top-K pages per
 (sequence, KV head), and run sparse paged decode over them (three library
-calls, five kernel launches).  Inputs are synthetic and resident in HBM (the KV pool exceeds
-the 129 MB L2, and the query rotates over 16 variants, so a step never finds
-its predecessor's selection in L2).
+calls, five kernel launches).  Inputs are synthetic and resident in HBM.  The
+query rotates over 16 variants, and where one step's K/V would fit in a few
+L2s the steps also rotate over copies of the KV pool and its metadata, so
+that a step never finds its K/V in the 129 MB L2.
+
+The JSON line's headline is the Llama-3-8B-like workload; `per_workload`
+carries the same measurement for the GPT2-345M-like, long-context,
+shared-prefix and tiny workloads.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     # the CPU oracle on the host cores
@@ -168,23 +173,6 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, or None
-    if the kernel source changed since the capture."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
-    src = os.path.join(ROOT, "query_aware_sparse_kv_gb300", "csrc", "decode.cu")
-    try:
-        text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    h = re.search(r"decode_cu_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != sha:
-        return None
-    return int(m.group(1))
-
-
 # ------------------------------------------------------------ distributed --
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -324,30 +312,56 @@ def run_reference(args):
 
 
 L2_BYTES = 129e6  # GB300 L2
+MAX_REPLICAS = 16
 
 
-def l2_note(inputs: dict) -> str:
-    """How the timed steps relate to L2: the KV pool's size and one step's
-    selected (or, dense, every) K/V bytes against the 129 MB L2."""
+def step_kv_bytes(inputs: dict) -> float:
+    """K+V bytes one step reads: the selected pages (sparse; top-K whole
+    pages per row), or every page once (dense; the shared prefix counted
+    once)."""
     spec = inputs["spec"]
-    pool = 2 * inputs["k_pool"].numel() * inputs["k_pool"].element_size()
     P, d, Hkv = spec.page_size, spec.head_dim, spec.num_kv_heads
     page = 2 * P * d * inputs["k_pool"].element_size()
     nb = inputs["n_pages"].long()
     pages = (torch.clamp(nb, max=spec.top_k) if spec.top_k is not None else nb).sum().item() * Hkv
     if spec.kind == "shared_prefix" and spec.top_k is None:
         pages = (nb.sum().item() - (spec.batch - 1) * spec.prefix_pages) * Hkv  # unique pages
-    step = pages * page
+    return float(pages * page)
+
+
+def replica_count(inputs: dict) -> int:
+    """Copies of the KV pool (and its metadata) the timed steps rotate over so
+    that consecutive steps never find their K/V in L2: enough that the K/V
+    the rotating steps read together exceeds 4 x L2 (a power of two, so the
+    16 query variants and the copies cycle together).  A workload whose
+    whole pool fits in L2 (the correctness case) is not replicated."""
+    pool = 2 * inputs["k_pool"].numel() * inputs["k_pool"].element_size()
+    if pool <= L2_BYTES:
+        return 1
+    r = 1
+    while r < MAX_REPLICAS and r * step_kv_bytes(inputs) < 4 * L2_BYTES:
+        r *= 2
+    return r
+
+
+def l2_note(inputs: dict, replicas: int = 1) -> str:
+    """How the timed steps relate to the 129 MB L2."""
+    pool = 2 * inputs["k_pool"].numel() * inputs["k_pool"].element_size()
+    step = step_kv_bytes(inputs)
     if pool <= L2_BYTES:
         return f"inputs fit in L2 (KV pool {pool / 1e6:.1f} MB; correctness workload), no flush"
-    if step > L2_BYTES:
-        return (f"KV pool {pool / 1e9:.2f} GB and one step's K/V {step / 1e6:.0f} MB both exceed L2; "
+    if replicas > 1:
+        return (f"KV pool {pool / 1e9:.2f} GB; one step reads {step / 1e6:.0f} MB of K/V, so the steps rotate over "
+                f"{replicas} copies of the pool and its metadata ({replicas * step / 1e6:.0f} MB of K/V >= 4 x L2): "
+                f"a step never finds its K/V in L2; 16 rotating query variants")
+    if step > 4 * L2_BYTES:
+        return (f"KV pool {pool / 1e9:.2f} GB and one step's K/V {step / 1e6:.0f} MB both exceed 4 x L2; "
                 f"16 rotating query variants")
-    return (f"KV pool {pool / 1e9:.2f} GB exceeds L2; one step's K/V ({step / 1e6:.0f} MB) fits in L2 and "
-            f"partly repeats across the 16 rotating query variants, as consecutive decode steps do; no flush")
+    return (f"KV pool {pool / 1e9:.2f} GB exceeds L2; one step's K/V ({step / 1e6:.0f} MB) is below 4 x L2 and "
+            f"partly repeats across the 16 rotating query variants (no pool copies)")
 
 
-def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None, inputs=None) -> dict:
+def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None, inputs=None, replicas: int = 1) -> dict:
     desc = {
         "llama3_8b": "Llama-3-8B-like GQA decode, query-aware top-K paged KV",
         "gpt2_345m": "GPT2-345M-like MHA decode at 8K, query-aware top-K paged KV",
@@ -364,11 +378,286 @@ def workload_config(spec: W.Spec, scorer: str = "bound", approx_eps=None, inputs
             "seq_len": list(spec.seq_len_range) if spec.seq_len_range else
             (list(spec.seq_lens)[:1] if spec.seq_lens else None),
             "top_k": spec.top_k, "kv_dtype": str(spec.kv_dtype).replace("torch.", ""),
-            "q_dtype": str(spec.q_dtype).replace("torch.", ""),
-            "l2": l2_note(inputs) if inputs is not None else "KV pool larger than L2, 16 rotating query variants"}
+            "q_dtype": str(spec.q_dtype).replace("torch.", ""), "pool_copies": replicas,
+            "l2": l2_note(inputs, replicas) if inputs is not None else
+            "KV pool larger than L2, 16 rotating query variants"}
+
+
+def source_hash(paths) -> str:
+    """Hash of the kernel sources with comments and blank lines removed, so a
+    comment-only edit keeps a profile's counters valid and a code edit does
+    not."""
+    h = hashlib.sha256()
+    for p in paths:
+        text = open(p).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(l.strip() for l in text.splitlines() if l.strip()).encode())
+    return h.hexdigest()[:16]
+
+
+DECODE_SOURCES = [os.path.join(ROOT, "query_aware_sparse_kv_gb300", "csrc", n)
+                  for n in ("decode.cu", "merge.cu", "qskv_device.cuh", "qskv_internal.h")]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, or None if
+    the decode kernel's code changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        text = open(path).read()
+        sha = source_hash(DECODE_SOURCES)
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = re.search(r"decode_src_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != sha:
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------- recall --
+def true_page_max_logits(inputs: dict, b: int, g: int, q) -> np.ndarray:
+    """max over the group's heads and the page's valid tokens of q_h . k_t,
+    per logical page of sequence b, KV head g (torch on the CPU, fp32): the
+    ground truth the bound's ranking is judged against."""
+    spec = inputs["spec"]
+    P, G = spec.page_size, spec.group
+    L = int(inputs["seq_lens"][b])
+    nb = (L + P - 1) // P
+    phys = inputs["page_table"][b, :nb].long()
+    keys = inputs["k_pool"][phys, g].float().reshape(nb * P, -1)[:L]  # tokens past seq_len dropped
+    logits = keys @ q[b, g * G:(g + 1) * G].float().T  # [L][G]
+    best = torch.full((nb * P,), float("-inf"))
+    best[:L] = logits.max(dim=1).values
+    return best.view(nb, P).max(dim=1).values.numpy()
+
+
+def selection_recall(inputs: dict, q, selected: np.ndarray, n_selected: np.ndarray, max_rows: int = 64) -> dict:
+    """Recall figures of the GPU's selection (one query variant):
+    true_topk: |selected & T| / K, T = the K pages with the largest true max
+               logit (TinyServe s2.2 states its recall this way), over rows
+               with more than K pages;
+    planted / aligned: share of the planted pages (Llama-like) or of the pages
+               drawn around the query's own centroid (long context) that are
+               kept, up to K."""
+    spec = inputs["spec"]
+    K, Hkv = spec.top_k, spec.num_kv_heads
+    rows = [(b, g) for b in range(spec.batch) for g in range(Hkv)]
+    rng = np.random.default_rng(0)
+    if len(rows) > max_rows:
+        rows = [rows[i] for i in sorted(rng.choice(len(rows), size=max_rows, replace=False))]
+    true_r, struct_r = [], []
+    struct = inputs.get("planted") if inputs.get("planted") is not None else inputs.get("aligned")
+    for b, g in rows:
+        sel = set(selected[b, g, :int(n_selected[b, g])].tolist())
+        nb = int(inputs["n_pages"][b])
+        if nb > K:
+            m = true_page_max_logits(inputs, b, g, q)
+            top = np.argsort(-m, kind="stable")[:K]
+            true_r.append(len(sel & set(top.tolist())) / K)
+        if struct is not None:
+            pages = [int(x) for x in struct[b, g].tolist() if x >= 0]
+            if pages:
+                struct_r.append(len(sel & set(pages)) / min(len(pages), K))
+    out = {"rows": len(rows), "true_topk": float(np.mean(true_r)) if true_r else None}
+    if struct is not None:
+        out["planted" if inputs.get("planted") is not None else "aligned"] = float(np.mean(struct_r))
+    return out
 
 
 # ------------------------------------------------------------------ main --
+class Bench:
+    """One workload's decode step on the GPU: inputs (replicated to defeat L2),
+    a PagedDecoder, one CUDA graph per query variant for the whole step and
+    split graphs (selection part, decode part) for the decode call alone."""
+
+    def __init__(self, spec: W.Spec, args, dev, prefix: int):
+        import query_aware_sparse_kv_gb300 as qskv
+
+        self.spec, self.args, self.dev, self.prefix = spec, args, dev, prefix
+        t0 = time.perf_counter()
+        inputs = W.make_inputs(spec)
+        self.inputs = inputs
+        self.qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
+        self.qv = self.qv_cpu.to(dev)
+        self.replicas = R = replica_count(inputs) if not args.no_replicas else 1
+        n_pool = inputs["num_pool_pages"]
+        k = inputs["k_pool"].to(dev)
+        v = inputs["v_pool"].to(dev)
+        if R > 1:
+            k, v = k.repeat(R, 1, 1, 1), v.repeat(R, 1, 1, 1)
+        pt = inputs["page_table"].to(dev)
+        self.tables = [torch.where(pt >= 0, pt + r * n_pool, pt).contiguous() for r in range(R)]
+        top_k = inputs["top_k"]
+        self.dec = qskv.PagedDecoder(inputs["q"].to(dev), k, v, self.tables[0], inputs["seq_lens"].to(dev), top_k,
+                                     prefix_pages=prefix, scorer=args.scorer, approx_epsilon=args.approx_eps,
+                                     approx_seed=args.seed)
+        ids, vt = W.all_pages(inputs)
+        ids_all = torch.cat([ids + r * n_pool for r in range(R)]).to(dev)
+        self.dec.build_meta(ids_all, vt.repeat(R).to(dev))
+        li, lv = W.last_pages(inputs)
+        self.last = [((li + r * n_pool).to(dev), lv.to(dev)) for r in range(R)]
+        self.dec.check()
+        self.setup_s = time.perf_counter() - t0
+
+    def table_for(self, v: int) -> int:
+        return v % self.replicas
+
+    def use(self, v: int):
+        self.dec.page_table = self.tables[self.table_for(v)]
+
+    def select_part(self, v: int):
+        if self.spec.top_k is not None:  # a dense decode reads no metadata: no refresh
+            self.use(v)
+            self.dec.build_meta(*self.last[self.table_for(v)])
+            self.dec.select(q=self.qv[v])
+
+    def decode_part(self, v: int):
+        self.use(v)
+        self.dec.decode(q=self.qv[v])
+
+    @staticmethod
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()  # first use outside capture (kernel attributes, descriptors)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def bytes_and_recall(self, want_recall: bool):
+        acc, recall = [], None
+        spec = self.spec
+        for v in range(N_Q_VARIANTS):
+            if spec.top_k is None:
+                acc.append(step_bytes(self.inputs, None, None, prefix_pages=self.prefix))
+                break
+            self.use(v)
+            self.dec.select(q=self.qv[v])
+            torch.cuda.synchronize()
+            sel, ns = self.dec.selected.cpu().numpy(), self.dec.n_selected.cpu().numpy()
+            acc.append(step_bytes(self.inputs, sel, ns, scorer=self.args.scorer))
+            if v == 0 and want_recall:
+                recall = selection_recall(self.inputs, self.qv_cpu[0], sel, ns)
+        self.nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
+        return recall
+
+    def build_graphs(self, warmup: int):
+        for i in range(warmup):
+            self.select_part(i % N_Q_VARIANTS)
+            self.decode_part(i % N_Q_VARIANTS)
+        self.dec.check()
+        torch.cuda.synchronize()
+        self.step_graphs = [self.capture(lambda v=v: (self.select_part(v), self.decode_part(v)))
+                            for v in range(N_Q_VARIANTS)]
+        self.sel_graphs = [self.capture(lambda v=v: self.select_part(v)) for v in range(N_Q_VARIANTS)]
+        self.dec_graphs = [self.capture(lambda v=v: self.decode_part(v)) for v in range(N_Q_VARIANTS)]
+        for i in range(warmup):
+            self.step_graphs[i % N_Q_VARIANTS].replay()
+        self.dec.check()
+        torch.cuda.synchronize()
+
+    def time_steps(self, steps: int, world: int) -> float:
+        """Device time (ms) of `steps` graph replays, events on the launching stream."""
+        stream = torch.cuda.current_stream()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(steps):
+            self.step_graphs[i % N_Q_VARIANTS].replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return start.elapsed_time(stop)
+
+    def time_decode_call(self, n: int) -> float:
+        """Mean device time (ms) of the decode call alone: events around the
+        decode graph, each replayed right after its own selection graph."""
+        stream = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            v = i % N_Q_VARIANTS
+            self.sel_graphs[v].replay()
+            ev[i][0].record(stream)
+            self.dec_graphs[v].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        self.dec.check()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def time_eager(self, n: int) -> float:
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            self.select_part(i % N_Q_VARIANTS)
+            self.decode_part(i % N_Q_VARIANTS)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        self.dec.check()
+        return e0.elapsed_time(e1) / n
+
+    def e2e(self, steps: int, warmup: int, world: int, zero_copy: bool) -> float:
+        """Steps/s through the public API: one graph per step recorded by
+        PagedDecoder.capture_step with pinned host q / out (the kernels read q
+        from and write out to host memory when zero_copy), the host waiting
+        for every step's output (PagedDecoder.wait)."""
+        dec, spec = self.dec, self.spec
+        q_host = self.qv_cpu.pin_memory()
+        q_dev = torch.empty_like(self.qv[0])
+        q_dev.copy_(self.qv[0])
+        out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+        graphs = []
+        for v in range(N_Q_VARIANTS):
+            self.use(v)
+            refresh = self.last[self.table_for(v)] if spec.top_k is not None else (None, None)
+            graphs.append(dec.capture_step(q_dev, *refresh, q_host=q_host[v], out_host=out_host,
+                                           zero_copy=zero_copy))
+        for i in range(min(steps, warmup)):
+            graphs[i % N_Q_VARIANTS]()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            graphs[i % N_Q_VARIANTS]()
+            dec.wait()
+        s = max_over_ranks(time.perf_counter() - t0, world, self.dev)
+        dec.check()
+        self.e2e_h2d = int(q_dev.numel() * q_dev.element_size())
+        self.e2e_d2h = int(out_host.numel() * out_host.element_size())
+        return world * steps / s
+
+
+def _prefix_for(spec: W.Spec, args) -> int:
+    return spec.prefix_pages if (spec.kind == "shared_prefix" and not args.no_cascade) else 0
+
+
+def cpu_baseline(inputs, qv_cpu, args, budget: float, single: bool) -> dict:
+    sps, cores, sample, _ = oracle_sample(inputs, qv_cpu, budget_s=budget, threads=os.cpu_count() or 1,
+                                          scorer=args.scorer)
+    cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample,
+           "cpu_model": cpu_model()}
+    if single:
+        sps1, _, sample1, _ = oracle_sample(inputs, qv_cpu, budget_s=max(1.0, budget / 4), threads=1,
+                                            scorer=args.scorer)
+        cpu["single_thread"] = {"value": sps1, "unit": "steps/s", "sample": sample1}
+    return cpu
+
+
+def summary(bn: Bench, ms_per_step: float, decode_ms: float, peak: float) -> dict:
+    decode_gbs = bn.nbytes["decode"] / (decode_ms * 1e-3) / 1e9
+    step_gbs = bn.nbytes["total"] / (ms_per_step * 1e-3) / 1e9
+    return {"steps_per_s": 1000.0 / ms_per_step, "ms_per_step": ms_per_step, "effective_gbs": step_gbs,
+            "hbm_frac_step": step_gbs / peak, "decode_ms": decode_ms, "decode_gbs": decode_gbs,
+            "decode_frac": decode_gbs / peak, "bytes_per_step": bn.nbytes}
+
+
 def run_gpu(args):
     import query_aware_sparse_kv_gb300 as qskv
     from query_aware_sparse_kv_gb300 import build as qbuild
@@ -384,71 +673,17 @@ def run_gpu(args):
         qbuild.build()
     barrier(world)
     qskv.load()
+    peaks = measured_peaks()
 
     spec = W.spec_for(args.workload)
     if args.batch:
         spec = W.spec_for(args.workload, batch=args.batch,
                           seq_lens=spec.seq_lens[:1] * args.batch if spec.seq_lens else None)
     spec = shard_spec(spec, rank)
-    inputs = W.make_inputs(spec)
-    qv_cpu = W.q_variants(inputs, N_Q_VARIANTS)
-    prefix = spec.prefix_pages if (spec.kind == "shared_prefix" and not args.no_cascade) else 0
-    dec = qskv.from_inputs(inputs, device=dev, prefix_pages=prefix, scorer=args.scorer,
-                           approx_epsilon=args.approx_eps, approx_seed=args.seed)
-    qv = qv_cpu.to(dev)
-    ids, vt = W.all_pages(inputs)
-    dec.build_meta(ids.to(dev), vt.to(dev))
-    last_ids, last_valid = (t.to(dev) for t in W.last_pages(inputs))
-    dec.check()
-    stream = torch.cuda.current_stream()
-
-    # algorithmic bytes: average over the query variants' selections
-    acc = []
-    for v in range(N_Q_VARIANTS):
-        if spec.top_k is not None:
-            dec.select(q=qv[v])
-            torch.cuda.synchronize()
-            acc.append(step_bytes(inputs, dec.selected.cpu().numpy(), dec.n_selected.cpu().numpy(),
-                                  scorer=args.scorer))
-        else:
-            acc.append(step_bytes(inputs, None, None, prefix_pages=prefix))
-            break
-    nbytes = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
-
-    def select_part(v):
-        if spec.top_k is not None:  # a dense decode reads no metadata: no refresh
-            dec.build_meta(last_ids, last_valid)
-            dec.select(q=qv[v])
-
-    def decode_part(v):
-        dec.decode(q=qv[v])
-
-    def capture(fn):
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()  # first use outside capture (kernel attributes, descriptors)
-        torch.cuda.current_stream().wait_stream(side)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
-    # eager warm-up, then one CUDA graph per query variant for the whole step
-    # (the way a serving loop launches a decode step), and split graphs
-    # (selection part, decode part) for timing the decode call alone
-    for i in range(args.warmup):
-        select_part(i % N_Q_VARIANTS)
-        decode_part(i % N_Q_VARIANTS)
-    dec.check()
-    torch.cuda.synchronize()
-    step_graphs = [capture(lambda v=v: (select_part(v), decode_part(v))) for v in range(N_Q_VARIANTS)]
-    sel_graphs = [capture(lambda v=v: select_part(v)) for v in range(N_Q_VARIANTS)]
-    dec_graphs = [capture(lambda v=v: decode_part(v)) for v in range(N_Q_VARIANTS)]
-    for i in range(args.warmup):
-        step_graphs[i % N_Q_VARIANTS].replay()
-    dec.check()
-    torch.cuda.synchronize()
+    prefix = _prefix_for(spec, args)
+    main = Bench(spec, args, dev, prefix)
+    recall = main.bytes_and_recall(want_recall=spec.top_k is not None and rank == 0 and not args.no_recall)
+    main.build_graphs(args.warmup)
 
     gpu_id = str(local)
     try:
@@ -457,133 +692,86 @@ def run_gpu(args):
         pass
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev) if args.flush_l2 else None
-    step_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)] if args.flush_l2 else None)
-    barrier(world)
-    torch.cuda.synchronize()
     wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:  # L2 emptied before the step; the write is outside the step's events
-            flush.fill_(float(i))
-            step_ev[i][0].record(stream)
-        step_graphs[i % N_Q_VARIANTS].replay()
-        if flush is not None:
-            step_ev[i][1].record(stream)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms = main.time_steps(args.steps, world)
     wall1 = time.time()
-    barrier(world)
-    elapsed_ms = (sum(a.elapsed_time(b) for a, b in step_ev) if flush is not None else start.elapsed_time(stop))
     clocks = None
+    decode_ms = main.time_decode_call(min(args.steps, 1000))
+    eager_ms = main.time_eager(min(args.steps, 300))
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * args.steps / (elapsed_ms / 1000.0)
+
+    # end to end through the public API (zero-copy default; copy nodes as a diagnostic)
+    e2e_steps = 0 if args.no_e2e else min(args.steps, 500)
+    e2e_value = main.e2e(e2e_steps, args.warmup, world, True) if e2e_steps else None
+    e2e_copy_nodes = main.e2e(e2e_steps, args.warmup, world, False) if e2e_steps else None
+
+    # the other workloads, each timed the same way (step graphs, decode call)
+    per_workload = {}
+    if args.per_workload and world == 1:
+        for name in [n for n in PER_WORKLOAD_ORDER if n != args.workload]:
+            ws = W.spec_for(name)
+            bn = Bench(ws, args, dev, _prefix_for(ws, args))
+            rec = bn.bytes_and_recall(want_recall=ws.top_k is not None and not args.no_recall)
+            bn.build_graphs(args.warmup)
+            t0 = time.time()
+            ms = bn.time_steps(args.sub_steps, 1) / args.sub_steps
+            t1 = time.time()
+            dms = bn.time_decode_call(min(args.sub_steps, 1000))
+            ent = summary(bn, ms, dms, peaks["hbm_gbs"])
+            ent["config"] = workload_config(ws, args.scorer, args.approx_eps, bn.inputs, bn.replicas)
+            ent["steps"] = args.sub_steps
+            ent["recall"] = rec
+            ent["kernels_per_step"] = 5 if ws.top_k is not None else (3 if bn.prefix else 2)
+            if sampler:
+                ent["clocks"] = sampler.summary(t0, t1)
+            if not args.no_cpu_baseline:
+                ent["cpu_baseline"] = cpu_baseline(bn.inputs, bn.qv_cpu, args, args.cpu_budget / 2, single=False)
+            per_workload[name] = ent
+            del bn
+            torch.cuda.empty_cache()
     if sampler:
         time.sleep(0.25)
         sampler.stop()
         clocks = sampler.summary(wall0, wall1)
 
-    # decode call alone: events around the decode graph of each step
-    n_dec = min(args.steps, 1000)
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
-    for i in range(n_dec):
-        v = i % N_Q_VARIANTS
-        sel_graphs[v].replay()
-        dec_ev[i][0].record(stream)
-        dec_graphs[v].replay()
-        dec_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
-
-    # the same step issued call by call from Python (launch-overhead diagnostic)
-    n_eager = min(args.steps, 300)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(n_eager):
-        select_part(i % N_Q_VARIANTS)
-        decode_part(i % N_Q_VARIANTS)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = e0.elapsed_time(e1) / n_eager
-    dec.check()
-    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1000.0)
-
-    # end to end through the public API: each step is one replay of a graph
-    # captured by PagedDecoder.capture_step with the host buffers: its
-    # kernels read the step's query from pinned host memory and write the
-    # output into pinned host memory (zero-copy over the host link); the host
-    # waits for it (PagedDecoder.wait, an event poll) before the next step (a
-    # serving loop needs the output to go on).
-    e2e_steps = 0 if args.no_e2e else min(args.steps, 500)
-    q_host = qv_cpu.pin_memory()
-    q_dev = torch.empty_like(qv[0])
-    q_dev.copy_(qv[0])
-    out_host = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
-    def e2e_run(zero_copy):
-        refresh = (last_ids, last_valid) if spec.top_k is not None else (None, None)
-        graphs = [dec.capture_step(q_dev, *refresh, q_host=q_host[v], out_host=out_host,
-                                   zero_copy=zero_copy) for v in range(N_Q_VARIANTS)]
-        for i in range(min(e2e_steps, args.warmup)):
-            graphs[i % N_Q_VARIANTS]()
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(e2e_steps):
-            graphs[i % N_Q_VARIANTS]()
-            dec.wait()
-        s = max_over_ranks(time.perf_counter() - t0, world, dev)
-        dec.check()
-        return world * e2e_steps / s
-
-    # the public API's default (zero-copy) is the e2e figure; the same step
-    # with host<->device copy nodes is reported beside it as a diagnostic
-    e2e_value = e2e_run(True) if e2e_steps else None
-    e2e_copy_nodes = e2e_run(False) if e2e_steps else None
-
     if rank != 0:
         return 0
-    peaks = measured_peaks()
-    decode_gbs = nbytes["decode"] / (decode_ms * 1e-3) / 1e9
-    step_gbs = nbytes["total"] / (ms_per_step * 1e-3) / 1e9
+    main_sum = summary(main, ms_per_step, decode_ms, peaks["hbm_gbs"])
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        sps, cores, sample, _ = oracle_sample(inputs, qv_cpu, budget_s=args.cpu_budget,
-                                              threads=os.cpu_count() or 1, scorer=args.scorer)
-        sps1, _, sample1, _ = oracle_sample(inputs, qv_cpu, budget_s=max(1.0, args.cpu_budget / 4), threads=1,
-                                            scorer=args.scorer)
-        cpu = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample,
-               "single_thread": {"value": sps1, "unit": "steps/s", "sample": sample1}, "cpu_model": cpu_model()}
+        cpu = cpu_baseline(main.inputs, main.qv_cpu, args, args.cpu_budget, single=True)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": dict(workload_config(spec, args.scorer, args.approx_eps, inputs),
-                       **({"l2": "L2 flushed (2 x 129 MB write) before every timed step; each step timed by its own events"}
-                          if args.flush_l2 else {})),
-        "effective_gbs": step_gbs,
-        "hbm_frac_step": step_gbs / peaks["hbm_gbs"],
-        "bytes_per_step": nbytes,
+        "config": workload_config(spec, args.scorer, args.approx_eps, main.inputs, main.replicas),
+        "effective_gbs": main_sum["effective_gbs"],
+        "hbm_frac_step": main_sum["hbm_frac_step"],
+        "bytes_per_step": main.nbytes,
         "roofline": {"kernel": ("decode_bf16_kernel + prefix_attend_kernel (qskv_cascade_paged_decode)" if prefix
-                                else "decode_bf16_kernel (qskv_sparse_paged_decode)"), "bound": "hbm",
-                     "achieved": decode_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": decode_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "decode_ms": decode_ms, "bytes_per_launch": nbytes["decode"],
-                     "traffic": ncu_traffic(args.workload)},
+                                else "decode_bf16_kernel + merge (qskv_sparse_paged_decode)"), "bound": "hbm",
+                     "achieved": main_sum["decode_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": main_sum["decode_frac"], "peak_source": peaks["source"],
+                     "decode_ms": decode_ms, "bytes_per_launch": main.nbytes["decode"],
+                     "traffic": ncu_traffic(args.workload), "decode_src_sha256_16": source_hash(DECODE_SOURCES)},
         "cpu_baseline": cpu,
+        "recall": recall,
         "step_launch": ("CUDA graph replay, one graph per query variant (meta refresh + selection + decode)"
                         if spec.top_k is not None else
                         "CUDA graph replay, one graph per query variant (dense decode: no metadata refresh or selection)"),
         "eager_ms_per_step": eager_ms,
-        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps, "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)", "copy_nodes_value": e2e_copy_nodes,
-                "h2d_bytes_per_step": int(q_dev.numel() * q_dev.element_size()),
-                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps,
+                "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to "
+                        "pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)",
+                "copy_nodes_value": e2e_copy_nodes,
+                "h2d_bytes_per_step": getattr(main, "e2e_h2d", 0), "d2h_bytes_per_step": getattr(main, "e2e_d2h", 0)},
         # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: decode and
         # merge only; cascade: + the shared-prefix kernel)
         "gpu_launches": (5 if spec.top_k is not None else (3 if prefix else 2)) * args.steps,
         "clocks": clocks,
+        "per_workload": per_workload or None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -591,6 +779,9 @@ def run_gpu(args):
 
         dist.destroy_process_group()
     return 0
+
+
+PER_WORKLOAD_ORDER = ["llama3_8b", "gpt2_345m", "long_context", "shared_prefix", "tiny"]
 
 
 def main(argv=None):
@@ -609,11 +800,16 @@ def main(argv=None):
     ap.add_argument("--approx-eps", type=float, default=None,
                     help="lossy top-K: stop once floor(eps * K) pages are undecided and sample them")
     ap.add_argument("--seed", type=int, default=0, help="seed of the lossy top-K's sampling")
-    ap.add_argument("--flush-l2", action="store_true",
-                    help="write 2 x L2 before every timed step and time each step by its own events (cold L2)")
+    ap.add_argument("--no-replicas", action="store_true",
+                    help="do not rotate over copies of the KV pool (study of the warm-L2 case)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --workload (profiling runs); by default the other workloads follow")
+    ap.add_argument("--sub-steps", type=int, default=1000, help="timed steps of each other workload")
+    ap.add_argument("--no-recall", action="store_true", help="skip the recall figures of the selection")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)
+    args.per_workload = not args.no_per_workload
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

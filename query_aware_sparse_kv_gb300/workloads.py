@@ -123,6 +123,9 @@ def make_inputs(spec: Spec) -> dict:
       top_k       int (or None for dense)
       planted     [B][Hkv][n] int32 logical pages given the planted key
                   offset (-1 padded), or None for other kinds
+      aligned     centroid kind: [B][Hkv][n] int32 logical pages whose
+                  offset is the centroid the group's query was drawn near
+                  (-1 padded), else None
       plus ``spec``.
     """
     g = torch.Generator().manual_seed(1_000_003 * spec.seed + 17)
@@ -194,9 +197,20 @@ def make_inputs(spec: Spec) -> dict:
         for b in range(B):
             for h in range(Hkv):
                 q[b, h * G:(h + 1) * G] = cent[h, star[b, h]] + 0.5 * q[b, h * G:(h + 1) * G]
+        lists = []
+        for b in range(B):
+            phys = table[b, :int(n_pages[b])].long()
+            lists.append([torch.nonzero(assign[phys, h] == star[b, h]).flatten() for h in range(Hkv)])
+        width = max(1, max(len(x) for row in lists for x in row))
+        aligned = torch.full((B, Hkv, width), -1, dtype=torch.int32)
+        for b in range(B):
+            for h in range(Hkv):
+                aligned[b, h, :len(lists[b][h])] = lists[b][h].to(torch.int32)
 
     if spec.kind != "planted":
         planted = None
+    if spec.kind != "centroid":
+        aligned = None
     q = q.to(spec.q_dtype)
     k = k.to(spec.kv_dtype)
     v = v.to(spec.kv_dtype)
@@ -212,7 +226,8 @@ def make_inputs(spec: Spec) -> dict:
 
     return dict(spec=spec, q=q, k_pool=k, v_pool=v, page_table=table,
                 seq_lens=seq_lens, n_pages=n_pages.to(torch.int32),
-                top_k=spec.top_k, max_pages=max_pages, num_pool_pages=n_pool, planted=planted)
+                top_k=spec.top_k, max_pages=max_pages, num_pool_pages=n_pool, planted=planted,
+                aligned=aligned)
 
 
 def q_variants(inputs: dict, count: int = 16, noise: float = 0.25, seed: int = 99) -> torch.Tensor:

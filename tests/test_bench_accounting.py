@@ -76,3 +76,45 @@ def test_l2_note_states_what_holds():
     llama = W.make_inputs(W.spec_for("llama3_8b", batch=2, seq_len_range=(30000, 32000)))
     assert "both exceed L2" not in bench.l2_note(llama)  # 2 x 8 rows x 128 pages x 8 KB = 17 MB a step
     assert "exceeds L2" in bench.l2_note(llama)
+
+
+def _shape_only(name, **kw):
+    """A workload's shapes without its values: the pool is a broadcast view
+    (no memory), which is all the replica count reads."""
+    spec = W.spec_for(name, **kw)
+    g = torch.Generator().manual_seed(5)
+    if spec.seq_lens is not None:
+        seq = torch.tensor(list(spec.seq_lens), dtype=torch.int32)
+    elif spec.kind == "shared_prefix":
+        seq = torch.full((spec.batch,), (spec.prefix_pages + spec.suffix_pages) * spec.page_size, dtype=torch.int32)
+    else:
+        lo, hi = spec.seq_len_range
+        seq = torch.randint(lo, hi + 1, (spec.batch,), generator=g).to(torch.int32)
+    nb = (seq + spec.page_size - 1) // spec.page_size
+    n_pool = int(nb.sum()) if spec.kind != "shared_prefix" else spec.prefix_pages + spec.batch * spec.suffix_pages
+    pool = torch.zeros(1, dtype=spec.kv_dtype).expand(n_pool, spec.num_kv_heads, spec.page_size, spec.head_dim)
+    return {"spec": spec, "k_pool": pool, "n_pages": nb, "seq_lens": seq}
+
+
+def test_pool_copies_make_the_rotating_kv_exceed_four_l2():
+    """Steps rotate over enough copies of the pool that the K/V they read
+    together exceeds 4 x 129 MB: Llama-like 268 MB a step -> 2 copies,
+    GPT2-like 81 MB -> 8, long context 67 MB -> 8; the shared-prefix batch
+    (545 MB of unique K/V) and the tiny batch (fits in L2) need none."""
+    for name, want in (("llama3_8b", 2), ("gpt2_345m", 8), ("long_context", 8), ("shared_prefix", 1),
+                       ("tiny", 1)):
+        inp = _shape_only(name)
+        r = bench.replica_count(inp)
+        assert r == want, (name, r, bench.step_kv_bytes(inp))
+        if r > 1:
+            assert r * bench.step_kv_bytes(inp) >= 4 * bench.L2_BYTES
+            assert (r // 2) * bench.step_kv_bytes(inp) < 4 * bench.L2_BYTES
+            assert "copies of the pool" in bench.l2_note(inp, r)
+
+
+def test_source_hash_ignores_comments(tmp_path):
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text("int f() { return 1; }  // one\n/* block\n comment */\n")
+    b.write_text("// another comment\nint f() { return 1; }\n\n")
+    c.write_text("int f() { return 2; }\n")
+    assert bench.source_hash([a]) == bench.source_hash([b]) != bench.source_hash([c])
