@@ -137,9 +137,10 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t i) {
     return z ^ (z >> 31);
 }
 
-// Ranks one row's scores (all threads of the CTA take part).
+// Ranks one row's scores (all NT threads of the CTA take part).
+template <int NT>
 __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *srow) {
-    constexpr int NT = kSelectThreads;
+    static_assert(NT == 128 || NT == 256, "ranking CTAs have 128 or 256 threads");
     constexpr int NW = NT / 32;
     __shared__ uint32_t s_keys[kSelectKeyCap];
     __shared__ uint32_t s_hist[256];
@@ -219,7 +220,7 @@ __device__ void select_row(const SelectArgs &a, int row, int n_b, const float *s
         if (a.need_max > 0 && need <= a.need_max) break;
         lo = hi > 8 ? hi - 8 : 0;
         const uint32_t mask = (1u << (hi - lo)) - 1u;
-        s_hist[tid] = 0u;  // NT == 256 bins
+        for (int i = tid; i < 256; i += NT) s_hist[i] = 0u;
         __syncthreads();
         const uint32_t want = shr32(prefix, hi);
         for (int i = tid; i < n_b; i += NT) {
@@ -389,34 +390,26 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a) {
     const int cap = a.max_pages * a.page_size;
     seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
     const int n_b = (seq + a.page_size - 1) / a.page_size;
-    select_row(a, row, n_b, a.scores + int64_t(row) * a.max_pages);
+    select_row<kSelectThreads>(a, row, n_b, a.scores + int64_t(row) * a.max_pages);
 }
 
 // ---------------------------------------------- scores on tensor cores --
-// Three CTAs per SM (168 registers): more metadata rows in flight per SM than
-// at two, measured faster on GB300 despite a small spill.
-// HINT: the metadata scan is larger than L2 and is read evict-first.
-template <int D, bool QF32, bool HINT>
-__global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
-    constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = lane & 3, gid = lane >> 2;
-    int w_page0;  // this warp's 32 pages: 2 groups of 16
-    RowInfo r;
-    if (a.head_quads > 0) {
-        r = row_info_head_major(a, w_page0);
-    } else {
-        r = row_info(a);
-        w_page0 = blockIdx.x * kScoreThreads + warp * 32;
-    }
-    float *srow = a.scores + int64_t(r.row) * a.max_pages;
-    if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
+// One warp scores 32 pages of a row: two groups of 16 pages, each a
+// (16 pages x 2D) . (2D x 8 heads) mma.sync product.  Lane (gid, t) loads
+// 16-byte chunks 4 kp + t (kp < NKP) of the metadata rows of pages gid and
+// gid + 8 of both groups, and the matching chunks of head gid's query.
+template <int D>
+struct BoundScanRegs {
+    static constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
+};
 
-    // Every load of the warp is issued before any is used: q, the page ids,
-    // then the metadata rows of both groups.
+// Query chunks of head `gid` of KV head g's group (zero past the group).
+template <int D, bool QF32>
+__device__ __forceinline__ void bound_load_q(const SelectArgs &a, int b, int g, uint4 (&qraw)[2 * D / 32][QF32 ? 2 : 1]) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    const int lane = threadIdx.x & 31, t = lane & 3, gid = lane >> 2;
     const bool head_ok = gid < a.group;
-    const int64_t qoff = (int64_t(r.b) * a.num_q_heads + int64_t(r.g) * a.group + (head_ok ? gid : 0)) * D;
-    uint4 qraw[NKP][QF32 ? 2 : 1];
+    const int64_t qoff = (int64_t(b) * a.num_q_heads + int64_t(g) * a.group + (head_ok ? gid : 0)) * D;
 #pragma unroll
     for (int kp = 0; kp < NKP; kp++) {
         const int c = 4 * kp + t;
@@ -429,30 +422,54 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
             qraw[kp][0] = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff + col);
         }
     }
-    const int32_t *trow = a.page_table + int64_t(r.b) * a.max_pages;
-    int jj[4], pp[4];
-    bool vv[4], bad[4];
+}
+
+// Logical pages (jj) and physical ids (pp) of this lane's four metadata rows
+// among the warp's 32 pages from w_page0: rows gid, gid + 8 of group 0,
+// then of group 1; vv: the page exists (j < n_b).
+__device__ __forceinline__ void bound_page_ids(const SelectArgs &a, int b, int w_page0, int n_b, int (&jj)[4],
+                                               int (&pp)[4], bool (&vv)[4]) {
+    const int gid = (threadIdx.x & 31) >> 2;
+    const int32_t *trow = a.page_table + int64_t(b) * a.max_pages;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {  // rows gid, gid+8 of group 0, then of group 1
+    for (int i = 0; i < 4; i++) {
         jj[i] = w_page0 + (i >> 1) * 16 + gid + (i & 1) * 8;
-        vv[i] = jj[i] < r.n_b;
+        vv[i] = jj[i] < n_b;
         pp[i] = vv[i] ? trow[jj[i]] : 0;
     }
+}
+
+// The lane's metadata chunks of its four rows (zero for absent or bad pages).
+template <int D, bool HINT>
+__device__ __forceinline__ void bound_load_meta(const SelectArgs &a, int g, const int (&pp)[4], const bool (&vv)[4],
+                                                bool (&bad)[4], uint4 (&av)[4][2 * D / 32], uint64_t policy) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    const int t = threadIdx.x & 3;
     const char *meta = static_cast<const char *>(a.meta);
-    const uint64_t meta_policy = HINT ? l2_evict_first_policy() : 0;
-    uint4 av[4][NKP];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         bad[i] = vv[i] && (pp[i] < 0 || pp[i] >= a.num_pool_pages);
-        const char *rowp = meta + (int64_t(bad[i] ? 0 : pp[i]) * a.num_kv_heads + r.g) * (2 * D * 2);
+        const char *rowp = meta + (int64_t(bad[i] ? 0 : pp[i]) * a.num_kv_heads + g) * (2 * D * 2);
 #pragma unroll
         for (int kp = 0; kp < NKP; kp++)
             av[i][kp] = !(vv[i] && !bad[i]) ? make_uint4(0, 0, 0, 0)
-                        : HINT ? ldg_stream_v4_hint(rowp + (4 * kp + t) * 16, meta_policy)
+                        : HINT ? ldg_stream_v4_hint(rowp + (4 * kp + t) * 16, policy)
                                : ldg_stream_v4(rowp + (4 * kp + t) * 16);
     }
     if ((bad[0] || bad[1] || bad[2] || bad[3]) && t == 0) raise_error(a.flags, kErrPageId);
+}
 
+// Row scores of the warp's 32 pages: the bound of every head of the group as
+// [m | M] . [q- | q+] on the tensor cores, the best head per page, stored to
+// srow[j] (-inf for a bad page id).
+template <int D, bool QF32>
+__device__ __forceinline__ void bound_score_store(const SelectArgs &a, const uint4 (&qraw)[2 * D / 32][QF32 ? 2 : 1],
+                                                  const uint4 (&av)[4][2 * D / 32], const int (&jj)[4],
+                                                  const bool (&vv)[4], const bool (&bad)[4], int w_page0, int n_b,
+                                                  float *srow) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    const int lane = threadIdx.x & 31, t = lane & 3, gid = lane >> 2;
+    const bool head_ok = gid < a.group;
     // B operand: the [q- | q+] column of head gid of the group, in the chunk
     // order this lane uses for the metadata rows.
     uint32_t bh[NKP][4], bl[NKP][4];
@@ -494,7 +511,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
 #pragma unroll
     for (int grp = 0; grp < 2; grp++) {
         const int ia = 2 * grp, ib = 2 * grp + 1;
-        if (w_page0 + grp * 16 >= r.n_b) break;  // warp-uniform: the group holds no page
+        if (w_page0 + grp * 16 >= n_b) break;  // warp-uniform: the group holds no page
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kp = 0; kp < NKP; kp++) {
@@ -519,6 +536,38 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
             if (vv[ib]) srow[jj[ib]] = bad[ib] ? NEG : sb;
         }
     }
+}
+
+// One CTA per (row, 128 pages) -- or, head-major, per (sequence, 32 pages,
+// 4 KV heads) -- then the separate ranking kernel.  Three CTAs per SM (168
+// registers): more metadata rows in flight per SM than at two, measured
+// faster on GB300 despite a small spill.
+// HINT: the metadata scan is larger than L2 and is read evict-first.
+template <int D, bool QF32, bool HINT>
+__global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    const int warp = threadIdx.x >> 5;
+    int w_page0;  // this warp's 32 pages: 2 groups of 16
+    RowInfo r;
+    if (a.head_quads > 0) {
+        r = row_info_head_major(a, w_page0);
+    } else {
+        r = row_info(a);
+        w_page0 = blockIdx.x * kScoreThreads + warp * 32;
+    }
+    float *srow = a.scores + int64_t(r.row) * a.max_pages;
+    if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
+
+    // Every load of the warp is issued before any is used: q, the page ids,
+    // then the metadata rows of both groups.
+    uint4 qraw[NKP][QF32 ? 2 : 1];
+    bound_load_q<D, QF32>(a, r.b, r.g, qraw);
+    int jj[4], pp[4];
+    bool vv[4], bad[4];
+    bound_page_ids(a, r.b, w_page0, r.n_b, jj, pp, vv);
+    uint4 av[4][NKP];
+    bound_load_meta<D, HINT>(a, r.g, pp, vv, bad, av, HINT ? l2_evict_first_policy() : 0);
+    bound_score_store<D, QF32>(a, qraw, av, jj, vv, bad, w_page0, r.n_b, srow);
 }
 
 // -------------------------------------------------- scores on CUDA cores --

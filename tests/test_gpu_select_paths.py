@@ -52,6 +52,10 @@ CASES = {
     "beyond_smem": lambda: W.make_inputs(W.Spec(name="long_rows", batch=2, num_q_heads=8, num_kv_heads=2,
                                                 head_dim=64, page_size=16, seq_lens=(16 * 4500 + 3, 16 * 4200),
                                                 top_k=200, kind="iid", seed=43)),
+    # many short rows (2200), some shorter than K: one ranking CTA per row
+    "many_rows": lambda: W.make_inputs(W.Spec(name="many_rows", batch=1100, num_q_heads=4, num_kv_heads=2,
+                                              head_dim=64, page_size=16, seq_len_range=(20, 700), top_k=12,
+                                              kind="iid", seed=44)),
 }
 
 
@@ -110,3 +114,27 @@ def _exact_vs_sort(inp, oracle_lib):
         n_b = PR.n_pages_of(inp, b)
         want, cnt = oracle_lib.select(s_w[b, g, :n_b].astype(np.float64), spec.top_k)
         assert n_w[b, g] == cnt and sel_w[b, g].tolist() == want.tolist()
+
+
+def test_ranking_repeats_exactly_on_one_workspace(oracle_lib):
+    """Calls on one workspace, alternating two queries, give identical
+    selections every time: nothing a call leaves in the workspace changes
+    the next call's result."""
+    inp = CASES["llama"]()
+    dec = qskv.from_inputs(inp)
+    ids, vt = oracle_lib.all_pages(inp)
+    dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    q2 = (inp["q"].float() * -1.0).to(inp["q"].dtype).cuda()
+    first = {}
+    for i in range(6):
+        q = dec.q if i % 2 == 0 else q2
+        dec.selected.fill_(-7)
+        dec.select(q=q)
+        dec.check()
+        torch.cuda.synchronize()
+        got = (dec.selected.clone(), dec.n_selected.clone())
+        if i < 2:
+            first[i % 2] = got
+        else:
+            assert torch.equal(got[0], first[i % 2][0]) and torch.equal(got[1], first[i % 2][1]), f"call {i}"
+    assert not torch.equal(first[0][0], first[1][0])
