@@ -2,8 +2,9 @@
 
 A step is one pass of the whole hot path over one batch: refresh the
 metadata of the page each sequence appends to, select the top-K pages per
-(sequence, KV head), and run sparse paged decode over them (three library
-calls, five kernel launches).  Inputs are synthetic and resident in HBM.  The
+(sequence, KV head), and run sparse paged decode over them (two library
+calls: the refresh runs inside the scoring launch; scoring, ranking, decode
+and, where the decode does not fold its split rows itself, a merge).  Inputs are synthetic and resident in HBM.  The
 query rotates over 16 variants, and where one step's K/V would fit in a few
 L2s the steps also rotate over copies of the KV pool and its metadata, so
 that a step never finds its K/V in the 129 MB L2.
@@ -510,8 +511,11 @@ class Bench:
     def select_part(self, v: int):
         if self.spec.top_k is not None:  # a dense decode reads no metadata: no refresh
             self.use(v)
-            self.dec.build_meta(*self.last[self.table_for(v)])
-            self.dec.select(q=self.qv[v])
+            if self.dec.can_refresh_in_select:  # the last pages' refresh inside the scoring launch
+                self.dec.select(q=self.qv[v], refresh_last=True)
+            else:
+                self.dec.build_meta(*self.last[self.table_for(v)])
+                self.dec.select(q=self.qv[v])
 
     def decode_part(self, v: int):
         self.use(v)
@@ -616,9 +620,10 @@ class Bench:
         graphs = []
         for v in range(N_Q_VARIANTS):
             self.use(v)
-            refresh = self.last[self.table_for(v)] if spec.top_k is not None else (None, None)
+            fused = spec.top_k is not None and dec.can_refresh_in_select
+            refresh = self.last[self.table_for(v)] if spec.top_k is not None and not fused else (None, None)
             graphs.append(dec.capture_step(q_dev, *refresh, q_host=q_host[v], out_host=out_host,
-                                           zero_copy=zero_copy))
+                                           zero_copy=zero_copy, refresh_last=fused))
         for i in range(min(steps, warmup)):
             graphs[i % N_Q_VARIANTS]()
         barrier(world)
@@ -632,6 +637,26 @@ class Bench:
         self.e2e_h2d = int(q_dev.numel() * q_dev.element_size())
         self.e2e_d2h = int(out_host.numel() * out_host.element_size())
         return world * steps / s
+
+
+def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bound", approx: bool = False) -> int:
+    """The library's launches in one step: metadata refresh (inside the
+    scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
+    (sparse only), decode, and the merge kernel unless the decode grid folds
+    its split rows itself (bf16 KV, no shared prefix, and a row's pieces fit
+    one warp's single round of loads: pieces x G x d / 128 <= 16, with the
+    grid's 2 CTAs x 6 warps per SM); a cascade adds the prefix kernel."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    rows = spec.batch * spec.num_kv_heads
+    spr = spec.top_k if spec.top_k is not None else inputs["page_table"].shape[1] - prefix
+    upw = max(1, -(-rows * spr // (2 * sms * 6)))
+    pieces = -(-spr // upw) + 1
+    fold = (spec.kv_dtype == torch.bfloat16 and prefix == 0
+            and pieces * max(1, spec.group * spec.head_dim // 128) <= 16)
+    # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV
+    fused_refresh = spec.kv_dtype == torch.bfloat16 and scorer == "bound" and not approx
+    n = ((2 if fused_refresh else 3) if spec.top_k is not None else 0) + 1 + (0 if fold else 1)
+    return n + (1 if prefix else 0)
 
 
 def _prefix_for(spec: W.Spec, args) -> int:
@@ -723,7 +748,7 @@ def run_gpu(args):
             ent["config"] = workload_config(ws, args.scorer, args.approx_eps, bn.inputs, bn.replicas)
             ent["steps"] = args.sub_steps
             ent["recall"] = rec
-            ent["kernels_per_step"] = 5 if ws.top_k is not None else (3 if bn.prefix else 2)
+            ent["kernels_per_step"] = kernels_per_step(ws, bn.inputs, bn.prefix, args.scorer, args.approx_eps is not None)
             if sampler:
                 ent["clocks"] = sampler.summary(t0, t1)
             if not args.no_cpu_baseline:
@@ -758,7 +783,8 @@ def run_gpu(args):
                      "traffic": ncu_traffic(args.workload), "decode_src_sha256_16": source_hash(DECODE_SOURCES)},
         "cpu_baseline": cpu,
         "recall": recall,
-        "step_launch": ("CUDA graph replay, one graph per query variant (meta refresh + selection + decode)"
+        "step_launch": ("CUDA graph replay, one graph per query variant (last-page metadata refresh inside the "
+                        "scoring launch + ranking + decode)"
                         if spec.top_k is not None else
                         "CUDA graph replay, one graph per query variant (dense decode: no metadata refresh or selection)"),
         "eager_ms_per_step": eager_ms,
@@ -767,9 +793,10 @@ def run_gpu(args):
                         "pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)",
                 "copy_nodes_value": e2e_copy_nodes,
                 "h2d_bytes_per_step": getattr(main, "e2e_h2d", 0), "d2h_bytes_per_step": getattr(main, "e2e_d2h", 0)},
-        # kernels per step: metadata refresh, scoring, ranking, decode, merge (dense: decode and
-        # merge only; cascade: + the shared-prefix kernel)
-        "gpu_launches": (5 if spec.top_k is not None else (3 if prefix else 2)) * args.steps,
+        # kernels per step: metadata refresh (fused into scoring where it can be), scoring, ranking,
+        # decode, merge (dense: decode and merge only; cascade: + the shared-prefix kernel; no merge
+        # when the decode folds its split rows)
+        "gpu_launches": kernels_per_step(spec, main.inputs, prefix, args.scorer, args.approx_eps is not None) * args.steps,
         "clocks": clocks,
         "per_workload": per_workload or None,
     }

@@ -8,6 +8,9 @@
  *   qskv_sparse_paged_decode softmax(q K^T * scale) V over the selected pages,
  *                            split over warps and merged by log-sum-exp
  *
+ * (qskv_page_select_refresh does the first two in one launch: the last
+ * pages' metadata refresh inside the scoring grid),
+ *
  * with an alternative block score (the mean key of each page, "Block Top-K"):
  *
  *   qskv_kv_centroid_build     per-page mean key (fp32)
@@ -120,9 +123,10 @@ typedef struct {
  * calls may share one buffer).  The workspace must be 256-byte aligned and
  * zero-filled once before first use (e.g. cudaMemsetAsync); every call
  * leaves it ready for the next one.  It holds the device error word, a
- * score buffer for callers that pass none, and the split partial outputs of
- * decode (one slot per row plus one per decode warp).  Calls sharing a
- * workspace must not run concurrently on different streams.
+ * counter per (sequence, KV head) row, a score buffer for callers that pass
+ * none, and the split partial outputs of decode (one slot per row plus one
+ * per decode warp).  Calls sharing a workspace must not run concurrently on
+ * different streams.
  * Returns 0 if the shape is invalid or the device cannot be queried.
  */
 size_t qskv_workspace_size(const qskv_shape *shape);
@@ -162,6 +166,28 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
                              const int32_t *page_table, const int32_t *seq_lens, const qskv_shape *shape,
                              int32_t top_k, int32_t *selected, int32_t *n_selected, float *scores,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Metadata refresh of the pages the sequences append to, fused with page
+ * selection (TinyServe s5.3: the metadata is refreshed at every decode step;
+ * s2.2-2.3: score every page, keep the top K).  For every sequence b with
+ * n_b >= 1 pages, its last page p = page_table[b][n_b - 1] holds
+ * valid = seq_len - (n_b - 1) * page_size tokens: meta[p][g] is recomputed
+ * from k_pool for every KV head g exactly as qskv_kv_meta_build does, and the
+ * selection then runs exactly as qskv_page_select, scoring that page with its
+ * new metadata.  The result is that of qskv_kv_meta_build over the last
+ * pages followed by qskv_page_select, in one launch less.
+ * meta is read and written ([num_pool_pages][num_kv_heads][2][head_dim],
+ * bf16); the other pages' metadata must be current (built once at prefill).
+ * A sequence's last page must not appear in another sequence's table (it is
+ * being written to).  bf16 KV only (QSKV_ERR_UNSUPPORTED otherwise: use the
+ * two calls); q fp32 or bf16.  Same workspace and device errors as
+ * qskv_page_select.
+ */
+qskv_status qskv_page_select_refresh(const void *q, qskv_dtype q_dtype, const void *k_pool, void *meta,
+                                     qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                     const qskv_shape *shape, int32_t top_k, int32_t *selected, int32_t *n_selected,
+                                     float *scores, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Block summaries for the Block Top-K scorer (Vortex sparse-attention digest,
@@ -231,6 +257,9 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
  *   lse[b][h] = log sum_t exp(l_t).
  * selected == NULL means every page j < n_b (exact dense paged decode);
  * n_selected and top_k are then ignored.  sm_scale == 0 means 1/sqrt(d).
+ * A row split over several decode warps is combined either by the last of
+ * those warps (when its pieces fit one warp's single round of loads; a
+ * per-row counter in the workspace picks that warp) or by a second kernel.
  * A sequence with no token gives out = 0 and lse = -inf.  lse may be NULL.
  * Device errors: a bad page id or selected index skips that page and flags
  * QSKV_ERR_DEVICE_INDEX.
@@ -249,13 +278,14 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
  * the device) is not allowed.  The pages have no counterpart of this call.
  *
  * Same arguments and results as qskv_sparse_paged_decode minus the
- * workspace.  The split partials and the error word live in an 8 MiB array
- * of device memory built into the library (every GPU that loads the library
- * holds it until the process exits).  A shape whose scratch (about 256 B +
- * (rows + 12 x SM count) x G x (head_dim + 1) x 4 B, rows = batch x
- * num_kv_heads) exceeds 8 MiB is rejected with QSKV_ERR_WORKSPACE before any
- * launch.  Each call clears the error word with cudaMemsetAsync on `stream`;
- * nothing is allocated or freed.  Device-side index errors still
+ * workspace.  The split partials, the row counters and the error word live
+ * in an 8 MiB array of device memory built into the library (every GPU that
+ * loads the library holds it until the process exits).  A shape whose
+ * scratch (about 256 B + rows x 4 B + (rows + 12 x SM count) x G x
+ * (head_dim + 1) x 4 B, rows = batch x num_kv_heads) exceeds 8 MiB is
+ * rejected with QSKV_ERR_WORKSPACE before any launch.  Each call clears the
+ * error word and the row counters with cudaMemsetAsync on `stream`; nothing
+ * is allocated or freed.  Device-side index errors still
  * skip the offending page but are not reported (no workspace to read them
  * from): use qskv_sparse_paged_decode to diagnose.
  * The first call on a device looks up the array's device address with that

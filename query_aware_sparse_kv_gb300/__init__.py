@@ -5,6 +5,8 @@ in include/qskv.h); this package is its binding:
 
   kv_meta_build        per-page min/max key metadata
   page_select          bound score of every page and top-K per (sequence, KV head)
+  page_select_refresh  the same, after rebuilding every sequence's last-page
+                       metadata in the same launch
   kv_centroid_build,   Block Top-K: per-page mean key, and q . centroid scores
   page_select_centroid   with the same top-K
   page_select_approx   either score with a lossy top-K (early exit + sampling)
@@ -19,12 +21,12 @@ built library every call raises.
 """
 from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, cascade_paged_decode,
                       cascade_workspace_size, get_error, kv_centroid_build, kv_meta_build, last_error_message, load,
-                      make_shape, page_select, page_select_approx, page_select_centroid, sparse_paged_decode,
+                      make_shape, page_select, page_select_approx, page_select_refresh, page_select_centroid, sparse_paged_decode,
                       sparse_paged_decode_noalloc, workspace_size)
 from .engine import PagedDecoder, from_inputs
 
 __all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "cascade_paged_decode",
            "cascade_workspace_size", "get_error", "kv_centroid_build", "kv_meta_build", "page_select_approx", "page_select_centroid",
-           "last_error_message", "load", "make_shape", "page_select", "sparse_paged_decode",
+           "last_error_message", "load", "make_shape", "page_select", "page_select_refresh", "sparse_paged_decode",
            "sparse_paged_decode_noalloc", "workspace_size",
            "PagedDecoder", "from_inputs"]

@@ -22,7 +22,8 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
           4: "QSKV_ERR_CUDA", 5: "QSKV_ERR_DEVICE_INDEX", 6: "QSKV_ERR_DEVICE_TIMEOUT"}
 
 # Every function the header declares, in declaration order.
-EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_kv_centroid_build",
+EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_page_select_refresh",
+           "qskv_kv_centroid_build",
            "qskv_page_select_centroid", "qskv_page_select_approx", "qskv_sparse_paged_decode",
            "qskv_sparse_paged_decode_noalloc", "qskv_cascade_workspace_size", "qskv_cascade_paged_decode",
            "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
@@ -67,6 +68,9 @@ def load(path: str = LIB_PATH):
     lib.qskv_page_select.restype = ctypes.c_int
     lib.qskv_page_select.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i32p, sp, i32, i32p, i32p, f32p, vp,
                                      sz, vp]
+    lib.qskv_page_select_refresh.restype = ctypes.c_int
+    lib.qskv_page_select_refresh.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32, i32p, i32p,
+                                             f32p, vp, sz, vp]
     lib.qskv_kv_centroid_build.restype = ctypes.c_int
     lib.qskv_kv_centroid_build.argtypes = [vp, ctypes.c_int, sp, i32p, i32p, i32, f32p, vp, sz, vp]
     lib.qskv_page_select_centroid.restype = ctypes.c_int
@@ -148,6 +152,17 @@ def page_select(q: torch.Tensor, meta: torch.Tensor, page_table: torch.Tensor, s
     _check(load().qskv_page_select(_ptr(q), _dtype(q), _ptr(meta), _dtype(meta), _ptr(page_table), _ptr(seq_lens),
                                    ctypes.byref(shape), int(top_k), _ptr(selected), _ptr(n_selected), _ptr(scores),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def page_select_refresh(q: torch.Tensor, k_pool: torch.Tensor, meta: torch.Tensor, page_table: torch.Tensor,
+                        seq_lens: torch.Tensor, top_k: int, selected: torch.Tensor, n_selected: torch.Tensor,
+                        shape: Shape, workspace: torch.Tensor, scores: Optional[torch.Tensor] = None, stream=None):
+    """The last page of every sequence gets its metadata rebuilt from k_pool,
+    then the selection runs (one launch less than kv_meta_build + page_select)."""
+    _check(load().qskv_page_select_refresh(_ptr(q), _dtype(q), _ptr(k_pool), _ptr(meta), _dtype(k_pool),
+                                           _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(top_k),
+                                           _ptr(selected), _ptr(n_selected), _ptr(scores), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def kv_centroid_build(k_pool: torch.Tensor, page_ids: torch.Tensor, valid_tokens: torch.Tensor,

@@ -116,6 +116,115 @@ __device__ void write_empty_piece(const DecodeArgs &a, int row, int64_t gw) {
     }
 }
 
+// Folds the pieces of split row `row` (slots row + w0 .. row + w1) into its
+// final output, with one warp (used when the pieces fit one round of loads,
+// kFoldMaxLoads): out = sum_w 2^(lse_w - m) o_w / sum_w 2^(lse_w - m),
+// m = max_w lse_w (log2 domain), exactly as the merge kernel.  Lane l folds
+// columns l, l + 32, ... of the row's G x D/4 float4 columns (CPL per lane),
+// BATCH pieces' loads in flight at a time.  Pieces are read from L2.
+template <int D, int G>
+__device__ void fold_row_warp(const DecodeArgs &a, int row, int64_t w0, int64_t w1) {
+    constexpr int V4 = D / 4;
+    constexpr int COLS = G * V4;
+    constexpr int CPL = COLS >= 32 ? COLS / 32 : 1;
+    constexpr int BATCH = 16 / CPL;
+    const int lane = threadIdx.x & 31;
+    if (COLS < 32 && lane >= COLS) return;
+    const int n = int(w1 - w0 + 1);
+    const int64_t slot0 = row + w0;
+    const float4 *o_all = reinterpret_cast<const float4 *>(a.part_o);
+    float mx[CPL], den[CPL];
+    float4 acc[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; j++) {
+        mx[j] = -INFINITY;
+        den[j] = 0.f;
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int p0 = 0; p0 < n; p0 += BATCH) {
+        float l[BATCH][CPL];
+        float4 v[BATCH][CPL];
+#pragma unroll
+        for (int k = 0; k < BATCH; k++)
+#pragma unroll
+            for (int j = 0; j < CPL; j++) {
+                const int c = lane + 32 * j;
+                const bool ok = p0 + k < n;
+                const int64_t s = slot0 + p0 + k;
+                l[k][j] = ok ? __ldcg(a.part_lse + s * G + c / V4) : -INFINITY;
+                v[k][j] = ok ? __ldcg(o_all + s * COLS + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int j = 0; j < CPL; j++) {
+            float m = mx[j];
+#pragma unroll
+            for (int k = 0; k < BATCH; k++) m = fmaxf(m, l[k][j]);
+            if (m == -INFINITY) continue;
+            const float sc = exp2f(mx[j] - m);
+            den[j] *= sc;
+            acc[j].x *= sc;
+            acc[j].y *= sc;
+            acc[j].z *= sc;
+            acc[j].w *= sc;
+#pragma unroll
+            for (int k = 0; k < BATCH; k++) {
+                if (l[k][j] == -INFINITY) continue;  // an empty piece: its o holds no data
+                const float w = exp2f(l[k][j] - m);
+                den[j] += w;
+                acc[j].x = fmaf(w, v[k][j].x, acc[j].x);
+                acc[j].y = fmaf(w, v[k][j].y, acc[j].y);
+                acc[j].z = fmaf(w, v[k][j].z, acc[j].z);
+                acc[j].w = fmaf(w, v[k][j].w, acc[j].w);
+            }
+            mx[j] = m;
+        }
+    }
+    const int b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+    const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+#pragma unroll
+    for (int j = 0; j < CPL; j++) {
+        const int c = lane + 32 * j, h = c / V4, c4 = c % V4;
+        const float inv = den[j] > 0.f ? 1.f / den[j] : 0.f;
+        reinterpret_cast<float4 *>(a.out + (qh0 + h) * D)[c4] =
+            make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+        if (c4 == 0 && a.lse) a.lse[qh0 + h] = den[j] > 0.f ? (mx[j] + log2f(den[j])) * kLn2 : -INFINITY;
+    }
+}
+
+// Ends a warp's work when the call folds split rows itself (no merge
+// kernel): the warp's pieces are made visible device-wide, then the warp
+// takes a ticket on each row it shares with other warps (only the first and
+// the last row of its range can be shared); the warp drawing a row's last
+// ticket has every other piece of the row visible and folds the row, then
+// resets the row's counter for the next call.  No warp waits for another.
+template <int D>
+__device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_last) {
+    const int lane = threadIdx.x & 31;
+    __threadfence();  // this lane's piece stores, before the tickets
+    __syncwarp();
+    for (int k = 0; k < 2; k++) {
+        const int row = k == 0 ? row_first : row_last;
+        if (k == 1 && row_last == row_first) break;
+        int64_t w0, w1;
+        row_warps(a, row, w0, w1);
+        if (row_is_final(a, w0, w1)) continue;  // this warp wrote the row's output itself
+        uint32_t last = 0;
+        if (lane == 0) {
+            last = atomicAdd(a.tickets + row, 1u) == uint32_t(w1 - w0) ? 1u : 0u;
+            if (last) __threadfence();  // the other warps' pieces, before they are read
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        switch (a.group) {
+            case 1: fold_row_warp<D, 1>(a, row, w0, w1); break;
+            case 2: fold_row_warp<D, 2>(a, row, w0, w1); break;
+            case 4: fold_row_warp<D, 4>(a, row, w0, w1); break;
+            default: fold_row_warp<D, 8>(a, row, w0, w1); break;
+        }
+        __syncwarp();
+        if (lane == 0) a.tickets[row] = 0u;
+    }
+}
+
 // A stage holds up to HALVES 16-token sub-tiles ("halves") of one row: K
 // then V, each half as D/64 boxes of 16 tokens x 64 dims (128-byte swizzle).
 // HINT: the call streams more K/V than L2 holds; the loads carry an
@@ -420,6 +529,8 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                     cphase ^= 1u;
                 }
             }
+            // keep the row counters consistent (the outputs are flagged as invalid)
+            if (a.fold) fold_shared_rows<D>(a, row_begin, row_last);
             if (a.wait_at_exit) pdl_wait();
             return;
         }
@@ -495,6 +606,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     if (cur_row >= 0) finish_row(cur_row);
     for (int r = empty_from; r <= row_last; r++)
         if (r != cur_row) write_empty_piece<D>(a, r, gw);
+    if (a.fold) fold_shared_rows<D>(a, row_begin, row_last);
     if (a.wait_at_exit) pdl_wait();
 }
 
@@ -690,6 +802,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
         if (a.total_units > 0) {
             DecodeArgs d = da;
             d.wait_at_exit = 1;
+            d.fold = 0;  // the prefix kernel's pieces are merged by the merge kernel
             if (head_dim == 128)
                 e = qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream)
                        : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream);
@@ -702,6 +815,14 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
     }
     if (a.total_units == 0) return cudaSuccess;
     if (kv_dtype == kDtypeBf16) {
+        // A split row is folded inside the decode grid by its last warp when
+        // that warp can fetch all the row's pieces in one round of loads (at
+        // most kFoldMaxLoads 16-byte loads per lane); otherwise the merge
+        // kernel, with a CTA per row, folds it.
+        const int64_t upw = a.units_per_warp > 0 ? a.units_per_warp : 1;
+        const int64_t pieces = (a.slots_per_row + upw - 1) / upw + 1;
+        const int64_t per_lane = a.group * head_dim / 128 > 1 ? a.group * head_dim / 128 : 1;
+        da.fold = a.tickets != nullptr && pieces * per_lane <= kFoldMaxLoads ? 1 : 0;
         cudaError_t e;
         if (head_dim == 128)
             e = qf ? launch_bf16<128, true>(da, tmap_k, tmap_v, grid, stream)
@@ -710,7 +831,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
             e = qf ? launch_bf16<64, true>(da, tmap_k, tmap_v, grid, stream)
                    : launch_bf16<64, false>(da, tmap_k, tmap_v, grid, stream);
         if (e != cudaSuccess) return e;
-        return launch_merge(a, head_dim, stream);
+        return da.fold ? cudaSuccess : launch_merge(a, head_dim, stream);
     }
     const dim3 g(grid.ctas), b(grid.warps_per_cta * 32);
     cudaError_t e;

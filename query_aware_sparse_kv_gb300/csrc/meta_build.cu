@@ -15,64 +15,9 @@
 namespace qskv {
 namespace {
 
-struct Bf16Ops {
-    using vec = uint4;  // 8 bf16
-    static __device__ __forceinline__ vec lowest() {
-        const uint32_t w = 0xff80ff80u;  // -inf, -inf
-        return make_uint4(w, w, w, w);
-    }
-    static __device__ __forceinline__ vec highest() {
-        const uint32_t w = 0x7f807f80u;  // +inf, +inf
-        return make_uint4(w, w, w, w);
-    }
-    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
-        __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
-        return *reinterpret_cast<uint32_t *>(&r);
-    }
-    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
-        __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
-        return *reinterpret_cast<uint32_t *>(&r);
-    }
-};
-
-struct F32Ops {
-    using vec = uint4;  // 4 fp32
-    static __device__ __forceinline__ vec lowest() {
-        const uint32_t w = 0xff800000u;
-        return make_uint4(w, w, w, w);
-    }
-    static __device__ __forceinline__ vec highest() {
-        const uint32_t w = 0x7f800000u;
-        return make_uint4(w, w, w, w);
-    }
-    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
-        return __float_as_uint(fminf(__uint_as_float(a), __uint_as_float(b)));
-    }
-    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
-        return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
-    }
-};
-
-template <class Ops>
-__device__ __forceinline__ uint4 vmin4(uint4 a, uint4 b) {
-    return make_uint4(Ops::vmin(a.x, b.x), Ops::vmin(a.y, b.y), Ops::vmin(a.z, b.z), Ops::vmin(a.w, b.w));
-}
-template <class Ops>
-__device__ __forceinline__ uint4 vmax4(uint4 a, uint4 b) {
-    return make_uint4(Ops::vmax(a.x, b.x), Ops::vmax(a.y, b.y), Ops::vmax(a.z, b.z), Ops::vmax(a.w, b.w));
-}
-
-__device__ __forceinline__ uint4 shfl_xor4(uint4 v, int m) {
-    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
-                      __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
-}
-
-// ROW_BYTES = D * element size; CPR = 16-byte chunks per token row.
+// ROW_BYTES = D * element size.
 template <class Ops, int ROW_BYTES>
 __global__ void __launch_bounds__(256) meta_build_kernel(MetaArgs a) {
-    constexpr int CPR = ROW_BYTES / 16;
-    constexpr int RP = 32 / CPR;  // token rows read in parallel by one warp
-    static_assert(CPR >= 1 && CPR <= 32 && 32 % CPR == 0, "row must be 16..512 bytes");
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -90,34 +35,7 @@ __global__ void __launch_bounds__(256) meta_build_kernel(MetaArgs a) {
         if (lane == 0) raise_error(a.flags, kErrValid);
         return;
     }
-    const int c = lane % CPR;
-    const int r0 = lane / CPR;
-    const uint8_t *base =
-        static_cast<const uint8_t *>(a.k_pool) + ((int64_t(p) * a.num_kv_heads + g) * a.page_size) * ROW_BYTES;
-    // every row load of the lane is issued before any is used (P <= 32)
-    constexpr int ITER = 32 / RP;
-    uint4 v[ITER];
-#pragma unroll
-    for (int i = 0; i < ITER; i++) {
-        const int r = r0 + i * RP;
-        v[i] = r < valid ? ldg_stream_v4(base + int64_t(r) * ROW_BYTES + c * 16) : Ops::highest();
-    }
-    uint4 mn = Ops::highest(), mx = Ops::lowest();
-#pragma unroll
-    for (int i = 0; i < ITER; i++) {
-        if (r0 + i * RP < valid) {
-            mn = vmin4<Ops>(mn, v[i]);
-            mx = vmax4<Ops>(mx, v[i]);
-        }
-    }
-#pragma unroll
-    for (int off = CPR; off < 32; off <<= 1) {
-        mn = vmin4<Ops>(mn, shfl_xor4(mn, off));
-        mx = vmax4<Ops>(mx, shfl_xor4(mx, off));
-    }
-    uint8_t *out = static_cast<uint8_t *>(a.meta) + (int64_t(p) * a.num_kv_heads + g) * 2 * ROW_BYTES;
-    if (r0 == 0) *reinterpret_cast<uint4 *>(out + c * 16) = mn;
-    if (r0 == (RP > 1 ? 1 : 0)) *reinterpret_cast<uint4 *>(out + ROW_BYTES + c * 16) = mx;
+    meta_tile_warp<Ops, ROW_BYTES>(a.k_pool, a.meta, p, g, valid, a.num_kv_heads, a.page_size);
 }
 
 // Block summary for the Block Top-K scorer (Vortex sparse-attention digest,

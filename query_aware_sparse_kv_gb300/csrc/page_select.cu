@@ -46,7 +46,7 @@ __device__ __forceinline__ uint32_t shr32(uint32_t x, int s) { return s >= 32 ? 
 
 // Row bookkeeping shared by both score kernels.
 struct RowInfo {
-    int row, b, g, n_b;
+    int row, b, g, n_b, seq;
 };
 
 __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
@@ -65,6 +65,7 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
         seq = seq < 0 ? 0 : cap;
     }
+    r.seq = seq;
     r.n_b = (seq + a.page_size - 1) / a.page_size;
     return r;
 }
@@ -89,6 +90,7 @@ __device__ __forceinline__ RowInfo row_info_head_major(const SelectArgs &a, int 
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
         seq = seq < 0 ? 0 : cap;
     }
+    r.seq = seq;
     r.n_b = (seq + a.page_size - 1) / a.page_size;
     return r;
 }
@@ -440,9 +442,12 @@ __device__ __forceinline__ void bound_page_ids(const SelectArgs &a, int b, int w
 }
 
 // The lane's metadata chunks of its four rows (zero for absent or bad pages).
+// The row of logical page fresh_j, just rewritten by this warp, is read
+// through L2 (the read-only path may hold its previous contents).
 template <int D, bool HINT>
 __device__ __forceinline__ void bound_load_meta(const SelectArgs &a, int g, const int (&pp)[4], const bool (&vv)[4],
-                                                bool (&bad)[4], uint4 (&av)[4][2 * D / 32], uint64_t policy) {
+                                                bool (&bad)[4], uint4 (&av)[4][2 * D / 32], uint64_t policy,
+                                                const int (&jj)[4], int fresh_j = -1) {
     constexpr int NKP = BoundScanRegs<D>::NKP;
     const int t = threadIdx.x & 3;
     const char *meta = static_cast<const char *>(a.meta);
@@ -450,11 +455,13 @@ __device__ __forceinline__ void bound_load_meta(const SelectArgs &a, int g, cons
     for (int i = 0; i < 4; i++) {
         bad[i] = vv[i] && (pp[i] < 0 || pp[i] >= a.num_pool_pages);
         const char *rowp = meta + (int64_t(bad[i] ? 0 : pp[i]) * a.num_kv_heads + g) * (2 * D * 2);
+        const bool fresh = jj[i] == fresh_j;
 #pragma unroll
         for (int kp = 0; kp < NKP; kp++)
             av[i][kp] = !(vv[i] && !bad[i]) ? make_uint4(0, 0, 0, 0)
-                        : HINT ? ldg_stream_v4_hint(rowp + (4 * kp + t) * 16, policy)
-                               : ldg_stream_v4(rowp + (4 * kp + t) * 16);
+                        : fresh ? __ldcg(reinterpret_cast<const uint4 *>(rowp + (4 * kp + t) * 16))
+                        : HINT  ? ldg_stream_v4_hint(rowp + (4 * kp + t) * 16, policy)
+                                : ldg_stream_v4(rowp + (4 * kp + t) * 16);
     }
     if ((bad[0] || bad[1] || bad[2] || bad[3]) && t == 0) raise_error(a.flags, kErrPageId);
 }
@@ -543,7 +550,12 @@ __device__ __forceinline__ void bound_score_store(const SelectArgs &a, const uin
 // registers): more metadata rows in flight per SM than at two, measured
 // faster on GB300 despite a small spill.
 // HINT: the metadata scan is larger than L2 and is read evict-first.
-template <int D, bool QF32, bool HINT>
+// REFRESH: first recompute the metadata of each row's last page from its
+// valid key rows (TinyServe s5.3: the page the new token went into), with the
+// warp that scores that page, which then scores it with the new rows.  The
+// CTAs take a sequence's pages from the last one backwards, so the refreshing
+// CTAs are among the first to run.
+template <int D, bool QF32, bool HINT, bool REFRESH>
 __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
     constexpr int NKP = BoundScanRegs<D>::NKP;
     const int warp = threadIdx.x >> 5;
@@ -551,9 +563,27 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
     RowInfo r;
     if (a.head_quads > 0) {
         r = row_info_head_major(a, w_page0);
+        if (REFRESH) {
+            const int nch = (r.n_b + 31) / 32, k = int(blockIdx.x) / a.head_quads;
+            w_page0 = k < nch ? (nch - 1 - k) * 32 : r.n_b;
+        }
     } else {
         r = row_info(a);
-        w_page0 = blockIdx.x * kScoreThreads + warp * 32;
+        if (REFRESH) {
+            const int nch = (r.n_b + kScoreThreads - 1) / kScoreThreads, k = int(blockIdx.x);
+            w_page0 = k < nch ? (nch - 1 - k) * kScoreThreads + warp * 32 : r.n_b;
+        } else {
+            w_page0 = blockIdx.x * kScoreThreads + warp * 32;
+        }
+    }
+    int fresh_j = -1;
+    if (REFRESH && r.n_b > 0 && r.n_b - 1 >= w_page0 && r.n_b - 1 < w_page0 + 32) {
+        fresh_j = r.n_b - 1;
+        const int p = a.page_table[int64_t(r.b) * a.max_pages + fresh_j];
+        if (p >= 0 && p < a.num_pool_pages)  // a bad id is flagged by the scan below
+            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, p, r.g, r.seq - fresh_j * a.page_size,
+                                            a.num_kv_heads, a.page_size);
+        __syncwarp();
     }
     float *srow = a.scores + int64_t(r.row) * a.max_pages;
     if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
@@ -566,7 +596,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs 
     bool vv[4], bad[4];
     bound_page_ids(a, r.b, w_page0, r.n_b, jj, pp, vv);
     uint4 av[4][NKP];
-    bound_load_meta<D, HINT>(a, r.g, pp, vv, bad, av, HINT ? l2_evict_first_policy() : 0);
+    bound_load_meta<D, HINT>(a, r.g, pp, vv, bad, av, HINT ? l2_evict_first_policy() : 0, jj, fresh_j);
     bound_score_store<D, QF32>(a, qraw, av, jj, vv, bad, w_page0, r.n_b, srow);
 }
 
@@ -763,7 +793,7 @@ cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int he
 }
 
 cudaError_t launch_page_select(const SelectArgs &a_in, int q_dtype, int meta_dtype, int head_dim,
-                               cudaStream_t stream, int score_all) {
+                               cudaStream_t stream, int score_all, int refresh) {
     const int64_t rows = int64_t(a_in.batch) * a_in.num_kv_heads;
     // a metadata scan larger than L2 is read evict-first (see launch_decode)
     SelectArgs a = a_in;
@@ -776,19 +806,25 @@ cudaError_t launch_page_select(const SelectArgs &a_in, int q_dtype, int meta_dty
                           : dim3(unsigned((a.max_pages + kScoreThreads - 1) / kScoreThreads), unsigned(rows));
     const dim3 block(kScoreThreads);
     const bool qf = q_dtype == kDtypeF32;
-    cudaError_t e;
+    cudaError_t e = cudaErrorInvalidValue;
     if (meta_dtype == kDtypeBf16) {
-        const bool h = a.meta_evict_first != 0;
+        auto go = [&](auto d_tag, auto q_tag, auto h_tag, auto r_tag) {
+            e = launch_pdl(score_mma_kernel<decltype(d_tag)::value, decltype(q_tag)::value, decltype(h_tag)::value,
+                                            decltype(r_tag)::value>,
+                           grid, block, 0, stream, a, score_all);
+        };
+        auto go_r = [&](auto d_tag, auto q_tag, auto h_tag) {
+            refresh ? go(d_tag, q_tag, h_tag, std::true_type()) : go(d_tag, q_tag, h_tag, std::false_type());
+        };
+        auto go_h = [&](auto d_tag, auto q_tag) {
+            a.meta_evict_first ? go_r(d_tag, q_tag, std::true_type()) : go_r(d_tag, q_tag, std::false_type());
+        };
+        using I64 = std::integral_constant<int, 64>;
+        using I128 = std::integral_constant<int, 128>;
         if (head_dim == 128)
-            e = qf ? (h ? launch_pdl(score_mma_kernel<128, true, true>, grid, block, 0, stream, a, score_all)
-                        : launch_pdl(score_mma_kernel<128, true, false>, grid, block, 0, stream, a, score_all))
-                   : (h ? launch_pdl(score_mma_kernel<128, false, true>, grid, block, 0, stream, a, score_all)
-                        : launch_pdl(score_mma_kernel<128, false, false>, grid, block, 0, stream, a, score_all));
+            qf ? go_h(I128(), std::true_type()) : go_h(I128(), std::false_type());
         else
-            e = qf ? (h ? launch_pdl(score_mma_kernel<64, true, true>, grid, block, 0, stream, a, score_all)
-                        : launch_pdl(score_mma_kernel<64, true, false>, grid, block, 0, stream, a, score_all))
-                   : (h ? launch_pdl(score_mma_kernel<64, false, true>, grid, block, 0, stream, a, score_all)
-                        : launch_pdl(score_mma_kernel<64, false, false>, grid, block, 0, stream, a, score_all));
+            qf ? go_h(I64(), std::true_type()) : go_h(I64(), std::false_type());
     } else {
         e = qf ? launch_pdl(score_simt_kernel<float, true>, grid, block, 0, stream, a, head_dim, score_all)
                : launch_pdl(score_simt_kernel<float, false>, grid, block, 0, stream, a, head_dim, score_all);

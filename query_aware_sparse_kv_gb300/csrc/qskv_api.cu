@@ -31,6 +31,8 @@ WorkspaceLayout workspace_layout(int64_t rows, int group, int head_dim, int max_
     size_t off = 0;
     w.flags = off;
     off += 256;
+    w.tickets = off;
+    off = align256(off + size_t(rows) * 4);
     w.scores = off;
     off = align256(off + size_t(rows) * size_t(max_pages) * 4);
     w.slots = rows + decode_grid(num_sms, head_dim).total_warps + rows * extra_per_row;
@@ -248,6 +250,8 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     SelectArgs a;
+    a.k_pool = nullptr;
+    a.meta_w = nullptr;
     a.q = q;
     a.meta = meta;
     a.page_table = page_table;
@@ -271,6 +275,59 @@ qskv_status qskv_page_select(const void *q, qskv_dtype q_dtype, const void *meta
     return launched(launch_page_select(a, q_dtype, meta_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
                                        scores != nullptr),
                     "page_select launch");
+}
+
+qskv_status qskv_page_select_refresh(const void *q, qskv_dtype q_dtype, const void *k_pool, void *meta,
+                                     qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                                     const qskv_shape *shape, int32_t top_k, int32_t *selected, int32_t *n_selected,
+                                     float *scores, void *workspace, size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (kv_dtype != QSKV_BF16)
+        return fail(QSKV_ERR_UNSUPPORTED, "the fused refresh needs a bf16 KV cache (use qskv_kv_meta_build + qskv_page_select)");
+    if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
+    if (!q || !k_pool || !meta || !page_table || !seq_lens || !selected || !n_selected)
+        return fail(QSKV_ERR_INVALID_ARG,
+                    "q, k_pool, meta, page_table, seq_lens, selected and n_selected must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(meta, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool and meta must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(scores, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index and score arrays must be 4-byte aligned");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    SelectArgs a;
+    a.k_pool = k_pool;
+    a.meta_w = meta;
+    a.q = q;
+    a.meta = meta;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.scores = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = top_k;
+    a.need_max = 0;
+    a.seed = 0;
+    a.meta_evict_first = 0;
+    a.head_quads = 0;
+    return launched(launch_page_select(a, q_dtype, kv_dtype, shape->head_dim, static_cast<cudaStream_t>(stream),
+                                       scores != nullptr, 1),
+                    "page_select_refresh launch");
 }
 
 qskv_status qskv_kv_centroid_build(const void *k_pool, qskv_dtype kv_dtype, const qskv_shape *shape,
@@ -324,6 +381,8 @@ qskv_status qskv_page_select_centroid(const void *q, qskv_dtype q_dtype, const f
     QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     SelectArgs a;
+    a.k_pool = nullptr;
+    a.meta_w = nullptr;
     a.q = q;
     a.meta = centroids;
     a.page_table = page_table;
@@ -377,6 +436,8 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
     QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     SelectArgs a;
+    a.k_pool = nullptr;
+    a.meta_w = nullptr;
     a.q = q;
     a.meta = meta;
     a.page_table = page_table;
@@ -459,6 +520,8 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
     a.wait_at_exit = 0;
     a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
+    a.tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
+    a.fold = 0;
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
     const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
@@ -499,9 +562,10 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     const int G = shape->num_q_heads / shape->num_kv_heads;
     const DecodeGrid grid = decode_grid(sms, shape->head_dim);
 
-    // Layout inside the static scratch: error word, then the partials.
+    // Layout inside the static scratch: error word, per-row counters, then the partials.
     const int64_t slots = rows + grid.total_warps;
-    const size_t off_part_o = 256;
+    const size_t off_tickets = 256;
+    const size_t off_part_o = align256(off_tickets + size_t(rows) * 4);
     const size_t off_part_lse = align256(off_part_o + size_t(slots) * G * shape->head_dim * 4);
     const size_t need = align256(off_part_lse + size_t(slots) * G * 4);
     if (need > kNoallocScratchBytes)
@@ -514,7 +578,7 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "cudaGetSymbolAddress of the decode scratch: %s", cudaGetErrorString(e));
     uint8_t *ws = static_cast<uint8_t *>(scratch);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the error word must start at zero on every call
+    // the error word and the row counters start at zero on every call
     e = cudaMemsetAsync(ws, 0, off_part_o, st);
     if (e != cudaSuccess) return fail(QSKV_ERR_CUDA, "clearing the decode scratch: %s", cudaGetErrorString(e));
 
@@ -546,6 +610,8 @@ qskv_status qskv_sparse_paged_decode_noalloc(const void *q, qskv_dtype q_dtype, 
     a.wait_at_exit = 0;
     a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
+    a.tickets = reinterpret_cast<uint32_t *>(ws + off_tickets);
+    a.fold = 0;
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
     const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
@@ -642,6 +708,8 @@ qskv_status qskv_cascade_paged_decode(const void *q, qskv_dtype q_dtype, const v
     a.wait_at_exit = 0;
     a.kv_evict_first = 0;
     a.stages = decode_stages(shape->head_dim);
+    a.tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
+    a.fold = 0;
     a.total_units = rows * a.slots_per_row;
     a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
     a.scale_log2 = scale * 1.4426950408889634f;

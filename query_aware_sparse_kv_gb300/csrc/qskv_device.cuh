@@ -342,6 +342,106 @@ __device__ __forceinline__ uint4 ldg_stream_v4_hint(const void *p, uint64_t poli
     return v;
 }
 
+// ------------------------------------------- element-wise min / max of keys --
+// The metadata of a page is the element-wise min and max of its key rows
+// (exact in the KV dtype); these are the operations every kernel that builds
+// it uses, so the results agree bit for bit.
+struct Bf16Ops {
+    using vec = uint4;  // 8 bf16
+    static __device__ __forceinline__ vec lowest() {
+        const uint32_t w = 0xff80ff80u;  // -inf, -inf
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ vec highest() {
+        const uint32_t w = 0x7f807f80u;  // +inf, +inf
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+};
+
+struct F32Ops {
+    using vec = uint4;  // 4 fp32
+    static __device__ __forceinline__ vec lowest() {
+        const uint32_t w = 0xff800000u;
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ vec highest() {
+        const uint32_t w = 0x7f800000u;
+        return make_uint4(w, w, w, w);
+    }
+    static __device__ __forceinline__ uint32_t vmin(uint32_t a, uint32_t b) {
+        return __float_as_uint(fminf(__uint_as_float(a), __uint_as_float(b)));
+    }
+    static __device__ __forceinline__ uint32_t vmax(uint32_t a, uint32_t b) {
+        return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+    }
+};
+
+template <class Ops>
+__device__ __forceinline__ uint4 vmin4(uint4 a, uint4 b) {
+    return make_uint4(Ops::vmin(a.x, b.x), Ops::vmin(a.y, b.y), Ops::vmin(a.z, b.z), Ops::vmin(a.w, b.w));
+}
+template <class Ops>
+__device__ __forceinline__ uint4 vmax4(uint4 a, uint4 b) {
+    return make_uint4(Ops::vmax(a.x, b.x), Ops::vmax(a.y, b.y), Ops::vmax(a.z, b.z), Ops::vmax(a.w, b.w));
+}
+
+__device__ __forceinline__ uint4 shfl_xor4(uint4 v, int m) {
+    return make_uint4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                      __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+
+// Metadata of one (page p, KV head g) tile with one warp: meta[p][g][0] =
+// element-wise min, meta[p][g][1] = max over the key rows t < valid.  Lanes
+// read the tile in 16-byte vectors, row-interleaved so a warp instruction
+// covers whole 128-byte lines (every row load of a lane issued before any is
+// used, page_size <= 32); each lane keeps a running min and max of its
+// vector column, lanes holding the same column combine by shuffles, and the
+// two rows are written as 16-byte vectors.  Min / max are exact, so any
+// evaluation order gives the same bits (up to the sign of zero).
+template <class Ops, int ROW_BYTES>
+__device__ __forceinline__ void meta_tile_warp(const void *k_pool, void *meta, int p, int g, int valid,
+                                               int num_kv_heads, int page_size) {
+    constexpr int CPR = ROW_BYTES / 16;  // 16-byte chunks per token row
+    constexpr int RP = 32 / CPR;         // token rows read in parallel by one warp
+    static_assert(CPR >= 1 && CPR <= 32 && 32 % CPR == 0, "row must be 16..512 bytes");
+    const int lane = threadIdx.x & 31;
+    const int c = lane % CPR;
+    const int r0 = lane / CPR;
+    const uint8_t *base =
+        static_cast<const uint8_t *>(k_pool) + ((int64_t(p) * num_kv_heads + g) * page_size) * ROW_BYTES;
+    constexpr int ITER = 32 / RP;
+    uint4 v[ITER];
+#pragma unroll
+    for (int i = 0; i < ITER; i++) {
+        const int r = r0 + i * RP;
+        v[i] = r < valid ? ldg_stream_v4(base + int64_t(r) * ROW_BYTES + c * 16) : Ops::highest();
+    }
+    uint4 mn = Ops::highest(), mx = Ops::lowest();
+#pragma unroll
+    for (int i = 0; i < ITER; i++) {
+        if (r0 + i * RP < valid) {
+            mn = vmin4<Ops>(mn, v[i]);
+            mx = vmax4<Ops>(mx, v[i]);
+        }
+    }
+#pragma unroll
+    for (int off = CPR; off < 32; off <<= 1) {
+        mn = vmin4<Ops>(mn, shfl_xor4(mn, off));
+        mx = vmax4<Ops>(mx, shfl_xor4(mx, off));
+    }
+    uint8_t *out = static_cast<uint8_t *>(meta) + (int64_t(p) * num_kv_heads + g) * 2 * ROW_BYTES;
+    if (r0 == 0) *reinterpret_cast<uint4 *>(out + c * 16) = mn;
+    if (r0 == (RP > 1 ? 1 : 0)) *reinterpret_cast<uint4 *>(out + ROW_BYTES + c * 16) = mx;
+}
+
 // ------------------------------------------------------- kernel arguments --
 struct MetaArgs {
     const void *k_pool;
@@ -355,6 +455,8 @@ struct MetaArgs {
 struct SelectArgs {
     const void *q;          // [B][Hq][D]
     const void *meta;       // [Npool][Hkv][2][D]
+    const void *k_pool;     // [Npool][Hkv][P][D] (metadata refresh of the last pages only)
+    void *meta_w;           // = meta, written by the refresh of the last pages
     const int32_t *page_table;
     const int32_t *seq_lens;
     int32_t *selected;      // [rows][top_k]
@@ -391,6 +493,8 @@ struct DecodeArgs {
                             // (the previous grid is the cascade's prefix kernel, which itself
                             // waited for everything before it)
     int32_t stages;
+    uint32_t *tickets;      // [rows] per-row counters of the in-grid fold (zero between calls)
+    int32_t fold;           // 1: split rows are folded by their last warp (no merge kernel)
     int64_t total_units;    // rows * slots_per_row
     int64_t units_per_warp; // ceil(total_units / total_warps)
     float scale_log2;       // sm_scale * log2(e)
@@ -469,5 +573,12 @@ constexpr int kDecodeWarpsD128 = QSKV_D128_WARPS, kDecodeHalvesD128 = QSKV_D128_
 constexpr int kDecodeWarpsD64 = QSKV_D64_WARPS, kDecodeHalvesD64 = QSKV_D64_HALVES,
               kDecodeStagesD64 = QSKV_D64_STAGES;
 constexpr int kMaxStages = 8;
+// The decode grid folds a split row itself when one warp can load all of the
+// row's pieces in a single round of at most this many 16-byte loads per lane
+// (pieces x G x D / 128).  Measured on GB300: the GPT2-like rows (15 pieces
+// of 64 floats) fold faster in the grid than in the merge kernel (decode call
+// 30.4 -> 29.0 us); the Llama-like rows (9 pieces of 4 x 128 floats, three
+// rounds for one warp) are slower that way (58.3 -> 61.9 us).
+constexpr int kFoldMaxLoads = 16;
 
 }  // namespace qskv

@@ -19,6 +19,7 @@ struct PrefixArgs;
 // Workspace layout: every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
     size_t flags;        // uint32 error word (+ padding to 256 B)
+    size_t tickets;      // uint32 [rows] per-row counters of the decode's fold (zero between calls)
     size_t scores;       // fp32  [rows][max_pages]
     size_t part_o;       // fp32  [slots][G][D]
     size_t part_lse;     // fp32  [slots][G]
@@ -47,8 +48,9 @@ cudaError_t launch_centroid_build(const MetaArgs &a, int kv_dtype, int head_dim,
 cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int head_dim, cudaStream_t stream,
                                         int score_all);
 // score_all: compute scores even for rows where every page is kept.
+// refresh: recompute each row's last-page metadata from a.k_pool first (bf16 only).
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
-                               int score_all);
+                               int score_all, int refresh = 0);
 // tmap_k / tmap_v are used by the bf16 tensor-core kernels only.  With
 // `prefix` (a cascade decode, bf16 KV) the shared-prefix kernel runs between
 // the decode and the merge.

@@ -70,7 +70,24 @@ class PagedDecoder:
             B.kv_meta_build(self.k_pool, page_ids, valid_tokens, self.meta, self.shape, self.workspace, stream)
 
     # -- indexer phase -------------------------------------------------------
-    def select(self, q=None, scores: Optional[torch.Tensor] = None, stream=None):
+    @property
+    def can_refresh_in_select(self) -> bool:
+        """Whether select(refresh_last=True) runs as one launch (bound scorer,
+        exact top-K, bf16 KV); otherwise it is a metadata build of the last
+        pages followed by the selection."""
+        return self.scorer == "bound" and self.approx_epsilon is None and self.k_pool.dtype == torch.bfloat16
+
+    def select(self, q=None, scores: Optional[torch.Tensor] = None, stream=None, refresh_last: bool = False):
+        """Top-K pages per (sequence, KV head).  refresh_last: first rebuild
+        the metadata of every sequence's last page (the page the new token
+        went into)."""
+        if refresh_last and self.can_refresh_in_select:
+            B.page_select_refresh(self.q if q is None else q, self.k_pool, self.meta, self.page_table, self.seq_lens,
+                                  self.top_k, self.selected, self.n_selected, self.shape, self.workspace, scores,
+                                  stream)
+            return
+        if refresh_last:
+            self.build_meta(*self._last_pages(), stream)
         if self.approx_epsilon is not None:
             B.page_select_approx(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k,
                                  self.selected, self.n_selected, self.shape, self.workspace, self.approx_epsilon,
@@ -79,6 +96,16 @@ class PagedDecoder:
         fn = B.page_select_centroid if self.scorer == "centroid" else B.page_select
         fn(self.q if q is None else q, self.meta, self.page_table, self.seq_lens, self.top_k, self.selected,
            self.n_selected, self.shape, self.workspace, scores, stream)
+
+    def _last_pages(self):
+        """(physical id, valid tokens) of every sequence's last page, gathered
+        on the device from the page table and the lengths (plumbing for the
+        two-call refresh; no arithmetic of the method)."""
+        P = self.shape.page_size
+        nb = torch.clamp((self.seq_lens.long() + P - 1) // P, min=1)
+        ids = self.page_table.gather(1, (nb - 1)[:, None]).squeeze(1).to(torch.int32)
+        valid = (self.seq_lens.long() - (nb - 1) * P).clamp(min=1).to(torch.int32)
+        return ids, valid
 
     def decode(self, q=None, dense: bool = False, out=None, lse=None, stream=None):
         sel = None if (dense or self.top_k is None) else self.selected
@@ -94,17 +121,19 @@ class PagedDecoder:
                               top_k=self.top_k or 0, lse=self.lse if lse is None else lse, sm_scale=self.sm_scale,
                               stream=stream)
 
-    def step(self, q=None, last_ids=None, last_valid=None, stream=None, out=None):
+    def step(self, q=None, last_ids=None, last_valid=None, stream=None, out=None, refresh_last: bool = False):
         """Metadata refresh of the pages being appended to, selection, decode
-        (into ``out`` if given, else ``self.out``)."""
+        (into ``out`` if given, else ``self.out``).  The refresh is either
+        the listed pages (last_ids, last_valid) or, with refresh_last, every
+        sequence's last page inside the selection's launch."""
         if last_ids is not None:
             self.build_meta(last_ids, last_valid, stream)
         if self.top_k is not None:
-            self.select(q, stream=stream)
+            self.select(q, stream=stream, refresh_last=refresh_last)
         self.decode(q, out=out, stream=stream)
 
     def capture_step(self, q: torch.Tensor, last_ids=None, last_valid=None, q_host: Optional[torch.Tensor] = None,
-                     out_host: Optional[torch.Tensor] = None, zero_copy: bool = True):
+                     out_host: Optional[torch.Tensor] = None, zero_copy: bool = True, refresh_last: bool = False):
         """Record one step (metadata refresh, selection, decode) reading the
         query from the device buffer `q` into a CUDA graph, and return a
         function that replays it on the current stream.  Refill `q` in place
@@ -122,11 +151,12 @@ class PagedDecoder:
         ``out_host`` last."""
         def body():
             if zero_copy:
-                self.step(q if q_host is None else q_host, last_ids, last_valid, out=out_host)
+                self.step(q if q_host is None else q_host, last_ids, last_valid, out=out_host,
+                          refresh_last=refresh_last)
                 return
             if q_host is not None:
                 q.copy_(q_host, non_blocking=True)
-            self.step(q, last_ids, last_valid)
+            self.step(q, last_ids, last_valid, refresh_last=refresh_last)
             if out_host is not None:
                 out_host.copy_(self.out, non_blocking=True)
 

@@ -96,6 +96,21 @@ def test_argument_checks(lib):
     assert lib.qskv_kv_meta_build(p, 1, ctypes.byref(shape), p, p, 0, p, p, 4096, None) == 0
 
 
+def test_refresh_select_argument_checks(lib):
+    """The fused refresh + selection rejects what it cannot do before any launch."""
+    shape = qskv.make_shape(2, 8, 2, 128, 16, 8, 16)
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    f = lib.qskv_page_select_refresh
+    assert f(p, 1, p, p, 0, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) == 2  # fp32 KV
+    assert f(p, 1, None, p, 1, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) == 1  # no k_pool
+    assert f(p, 1, p, p, 1, p, p, ctypes.byref(shape), 0, p, p, None, p, 4096, None) == 1  # top_k 0
+    assert f(p, 1, ctypes.c_void_p(base + 8), p, 1, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) == 1
+    assert "bf16" in (f(p, 1, p, p, 0, p, p, ctypes.byref(shape), 4, p, p, None, p, 4096, None) and
+                      lib.qskv_last_error_message().decode())
+
+
 def test_cascade_argument_checks(lib):
     shape = qskv.make_shape(2, 8, 2, 128, 16, 8, 16)
     buf = ctypes.create_string_buffer(1 << 16)
