@@ -356,7 +356,6 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             if (nh == 0) break;
             if (lane == 0) {
                 uint8_t *st = ring + size_t(ps) * STAGE;
-                fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar + ps, uint32_t(nh) * 2 * HALF);
 #pragma unroll
                 for (int nb = 0; nb < NB; nb++) {
@@ -456,53 +455,66 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         }
     };
 
-    // Q.K^T of NH halves (tokens gid / gid+8 x heads 2t / 2t+1), masked;
-    // the halves' accumulation chains are interleaved.
-    auto mask_scale = [&](const float (&sa)[2][4], int valid, float (&s)[4]) {
+    // Q.K^T of NH halves (tokens gid / gid+8 x heads 2t / 2t+1), masked.
+    // Every ldmatrix of a half is issued before its first mma, and the
+    // mma land on four accumulators in turn (short dependency chains).
+    constexpr int NCH = 4;
+    auto mask_scale = [&](const float (&sa)[NCH][4], int valid, float (&s)[4]) {
         const float sc = a.scale_log2;
-        s[0] = gid < valid ? (sa[0][0] + sa[1][0]) * sc : -INFINITY;
-        s[1] = gid < valid ? (sa[0][1] + sa[1][1]) * sc : -INFINITY;
-        s[2] = gid + 8 < valid ? (sa[0][2] + sa[1][2]) * sc : -INFINITY;
-        s[3] = gid + 8 < valid ? (sa[0][3] + sa[1][3]) * sc : -INFINITY;
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) x[i] = (sa[0][i] + sa[1][i]) + (sa[2][i] + sa[3][i]);
+        s[0] = gid < valid ? x[0] * sc : -INFINITY;
+        s[1] = gid < valid ? x[1] * sc : -INFINITY;
+        s[2] = gid + 8 < valid ? x[2] * sc : -INFINITY;
+        s[3] = gid + 8 < valid ? x[3] * sc : -INFINITY;
     };
     auto qk = [&](auto nh_tag, uint32_t kb, int v0, int v1, float (&s0)[4], float (&s1)[4]) {
         constexpr int NH = decltype(nh_tag)::value;
-        float sa[NH][2][4];
+        float sa[NH][NCH][4];
 #pragma unroll
         for (int h = 0; h < NH; h++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) sa[h][0][i] = sa[h][1][i] = 0.f;
+            for (int c = 0; c < NCH; c++)
+#pragma unroll
+                for (int i = 0; i < 4; i++) sa[h][c][i] = 0.f;
         const int mat = lane >> 3;
         const int r = (lane & 7) + ((mat & 1) << 3);
+        uint32_t af[NH][NKS][4];
 #pragma unroll
         for (int ks = 0; ks < NKS; ks++) {
             const int c = (ks & 3) * 2 + (mat >> 1);
             const uint32_t off = (ks >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4);
-            uint32_t af[NH][4];
 #pragma unroll
-            for (int h = 0; h < NH; h++) ldmatrix_x4(af[h], kb + h * HALF + off);
+            for (int h = 0; h < NH; h++) ldmatrix_x4(af[h][ks], kb + h * HALF + off);
+        }
+#pragma unroll
+        for (int ks = 0; ks < NKS; ks++)
 #pragma unroll
             for (int h = 0; h < NH; h++) {
-                mma_bf16_16816(sa[h][ks & 1], af[h], qb[ks][0], qb[ks][1]);
-                if (QF32) mma_bf16_16816(sa[h][ks & 1], af[h], ql[ks][0], ql[ks][1]);
+                mma_bf16_16816(sa[h][(QF32 ? 2 * ks : ks) % NCH], af[h][ks], qb[ks][0], qb[ks][1]);
+                if (QF32) mma_bf16_16816(sa[h][(2 * ks + 1) % NCH], af[h][ks], ql[ks][0], ql[ks][1]);
             }
-        }
         mask_scale(sa[0], v0, s0);
         if (NH == 2) mask_scale(sa[NH - 1], v1, s1);
     };
-    // O^T += V^T . P^T for one half.
+    // O^T += V^T . P^T for one half (the V fragments all loaded first).
     auto pv_half = [&](uint32_t vb, uint32_t pb0, uint32_t pb1) {
         const int mat = lane >> 3;
         const int r = (lane & 7) + ((mat >> 1) << 3);
+        uint32_t af[NKS][4];
 #pragma unroll
         for (int mt = 0; mt < NKS; mt++) {
             const int c = (mt & 3) * 2 + (mat & 1);
-            uint32_t af[4];
-            ldmatrix_x4_trans(af, vb + (mt >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
-            mma_bf16_16816(o[mt], af, pb0, pb1);
+            ldmatrix_x4_trans(af[mt], vb + (mt >> 2) * BOX + r * 128 + ((c ^ (r & 7)) << 4));
         }
+#pragma unroll
+        for (int mt = 0; mt < NKS; mt++) mma_bf16_16816(o[mt], af[mt], pb0, pb1);
     };
     // Zero the V rows of a half past its valid tokens (they may hold NaN).
+    // The stores are ordered before the stage's next TMA refill by a proxy
+    // fence (a refill only overwrites data the warp has read, which needs
+    // none).
     auto zero_v_tail = [&](uint8_t *vhalf, int valid) {
         uint4 *vrow = reinterpret_cast<uint4 *>(vhalf);
         const int n = (16 - valid) * 8;
@@ -510,6 +522,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             const int nb = i / n, r = valid + (i % n) / 8, c = i % 8;
             vrow[(nb * BOX + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
     };
 
     // ---------------- main loop: one stage (up to 32 tokens of one row) per pass
@@ -558,17 +571,18 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             qk(std::integral_constant<int, 1>(), kb, v0, v1, s0, s1);
             s1[0] = s1[1] = s1[2] = s1[3] = -INFINITY;
         }
-        // s*[0], s*[2]: head 2t; s*[1], s*[3]: head 2t+1
+        // s*[0], s*[2]: head 2t; s*[1], s*[3]: head 2t+1.  Lazy rescale: the
+        // running max moves only when some head's new max exceeds it by more
+        // than kLazy (then probabilities stay <= 2^kLazy); the per-lane maxima
+        // are tested first, so the cross-lane reduction runs only then.
         float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
         float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        // lazy rescale: keep the running max unless some head's new max
-        // exceeds it by more than kLazy (then probabilities stay <= 2^kLazy)
         if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
             const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
             const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
             m0 = n0;
