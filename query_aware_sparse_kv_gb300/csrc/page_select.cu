@@ -70,31 +70,6 @@ __device__ __forceinline__ RowInfo row_info(const SelectArgs &a) {
     return r;
 }
 
-// Head-major grid of the bound scan (num_kv_heads a multiple of 4): CTA
-// (x, b) covers the 32 pages from 32 (x / Q) of sequence b for KV heads
-// 4 (x % Q) .. 4 (x % Q) + 3, one head per warp (Q = num_kv_heads / 4), so
-// the CTAs x .. x + Q - 1, launched back to back, read a page's metadata rows
-// for all heads (contiguous in the [page][head] layout) at about the same
-// time.  page0: the warp's first page.
-__device__ __forceinline__ RowInfo row_info_head_major(const SelectArgs &a, int &page0) {
-    pdl_wait();
-    RowInfo r;
-    const int warp = threadIdx.x >> 5;
-    r.b = blockIdx.y;
-    r.g = (blockIdx.x % a.head_quads) * 4 + warp;
-    r.row = r.b * a.num_kv_heads + r.g;
-    page0 = (blockIdx.x / a.head_quads) * 32;
-    int seq = a.seq_lens[r.b];
-    const int cap = a.max_pages * a.page_size;
-    if (seq < 0 || seq > cap) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
-        seq = seq < 0 ? 0 : cap;
-    }
-    r.seq = seq;
-    r.n_b = (seq + a.page_size - 1) / a.page_size;
-    return r;
-}
-
 // --------------------------------------------------------------- select --
 // Exclusive block scans of x and y; total_y gets the sum of y over the block.
 template <int NT>
@@ -428,7 +403,9 @@ __device__ __forceinline__ void bound_load_q(const SelectArgs &a, int b, int g, 
 
 // Logical pages (jj) and physical ids (pp) of this lane's four metadata rows
 // among the warp's 32 pages from w_page0: rows gid, gid + 8 of group 0,
-// then of group 1; vv: the page exists (j < n_b).
+// then of group 1; vv: j < n_b.  The table row holds max_pages entries, so
+// the ids can be read with n_b = max_pages before the sequence length is
+// known (vv is then recomputed and the ids past the length are not used).
 __device__ __forceinline__ void bound_page_ids(const SelectArgs &a, int b, int w_page0, int n_b, int (&jj)[4],
                                                int (&pp)[4], bool (&vv)[4]) {
     const int gid = (threadIdx.x & 31) >> 2;
@@ -545,8 +522,11 @@ __device__ __forceinline__ void bound_score_store(const SelectArgs &a, const uin
     }
 }
 
-// One CTA per (row, 128 pages) -- or, head-major, per (sequence, 32 pages,
-// 4 KV heads) -- then the separate ranking kernel.  Three CTAs per SM (168
+// One CTA per (row, 128 pages) -- or, head-major (num_kv_heads a multiple of
+// 4), per (sequence, 32 pages, 4 KV heads): warp w takes KV head 4 (x % Q) + w
+// (Q = num_kv_heads / 4), so neighbouring CTAs read a page's metadata rows
+// for all heads (contiguous in the [page][head] layout) at about the same
+// time -- then the separate ranking kernel.  Three CTAs per SM (168
 // registers): more metadata rows in flight per SM than at two, measured
 // faster on GB300 despite a small spill.
 // HINT: the metadata scan is larger than L2 and is read evict-first.
@@ -559,45 +539,55 @@ template <int D, bool QF32, bool HINT, bool REFRESH>
 __global__ void __launch_bounds__(kScoreThreads, 3) score_mma_kernel(SelectArgs a, int score_all) {
     constexpr int NKP = BoundScanRegs<D>::NKP;
     const int warp = threadIdx.x >> 5;
-    int w_page0;  // this warp's 32 pages: 2 groups of 16
-    RowInfo r;
+    // The warp's row and pages follow from the block index alone, so the
+    // sequence length, the query and the page ids (the table row holds
+    // max_pages entries whatever the length) are requested together, and the
+    // metadata right after: two dependent round trips per CTA.  REFRESH
+    // counts the chunks back from max_pages, so a sequence's last chunk is its
+    // first CTA with pages.
+    int b, g, w_page0;  // w_page0: this warp's 32 pages (2 groups of 16)
     if (a.head_quads > 0) {
-        r = row_info_head_major(a, w_page0);
-        if (REFRESH) {
-            const int nch = (r.n_b + 31) / 32, k = int(blockIdx.x) / a.head_quads;
-            w_page0 = k < nch ? (nch - 1 - k) * 32 : r.n_b;
-        }
+        b = blockIdx.y;
+        g = (int(blockIdx.x) % a.head_quads) * 4 + warp;
+        const int k = int(blockIdx.x) / a.head_quads, nk = int(gridDim.x) / a.head_quads;
+        w_page0 = (REFRESH ? nk - 1 - k : k) * 32;
     } else {
-        r = row_info(a);
-        if (REFRESH) {
-            const int nch = (r.n_b + kScoreThreads - 1) / kScoreThreads, k = int(blockIdx.x);
-            w_page0 = k < nch ? (nch - 1 - k) * kScoreThreads + warp * 32 : r.n_b;
-        } else {
-            w_page0 = blockIdx.x * kScoreThreads + warp * 32;
-        }
+        b = int(blockIdx.y) / a.num_kv_heads;
+        g = int(blockIdx.y) % a.num_kv_heads;
+        w_page0 = (REFRESH ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x)) * kScoreThreads + warp * 32;
     }
-    int fresh_j = -1;
-    if (REFRESH && r.n_b > 0 && r.n_b - 1 >= w_page0 && r.n_b - 1 < w_page0 + 32) {
-        fresh_j = r.n_b - 1;
-        const int p = a.page_table[int64_t(r.b) * a.max_pages + fresh_j];
-        if (p >= 0 && p < a.num_pool_pages)  // a bad id is flagged by the scan below
-            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, p, r.g, r.seq - fresh_j * a.page_size,
-                                            a.num_kv_heads, a.page_size);
-        __syncwarp();
-    }
-    float *srow = a.scores + int64_t(r.row) * a.max_pages;
-    if (w_page0 >= r.n_b || (a.top_k >= r.n_b && !score_all)) return;
-
-    // Every load of the warp is issued before any is used: q, the page ids,
-    // then the metadata rows of both groups.
+    const int row = b * a.num_kv_heads + g;
+    pdl_wait();
+    int seq = a.seq_lens[b];
     uint4 qraw[NKP][QF32 ? 2 : 1];
-    bound_load_q<D, QF32>(a, r.b, r.g, qraw);
+    bound_load_q<D, QF32>(a, b, g, qraw);
     int jj[4], pp[4];
     bool vv[4], bad[4];
-    bound_page_ids(a, r.b, w_page0, r.n_b, jj, pp, vv);
+    bound_page_ids(a, b, w_page0, a.max_pages, jj, pp, vv);
+    const int cap = a.max_pages * a.page_size;
+    if (seq < 0 || seq > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) raise_error(a.flags, kErrSeqLen);
+        seq = seq < 0 ? 0 : cap;
+    }
+    const int n_b = (seq + a.page_size - 1) / a.page_size;
+#pragma unroll
+    for (int i = 0; i < 4; i++) vv[i] = jj[i] < n_b;
+
+    int fresh_j = -1;
+    if (REFRESH && n_b > 0 && n_b - 1 >= w_page0 && n_b - 1 < w_page0 + 32) {
+        fresh_j = n_b - 1;
+        const int p = a.page_table[int64_t(b) * a.max_pages + fresh_j];
+        if (p >= 0 && p < a.num_pool_pages)  // a bad id is flagged by the scan below
+            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, p, g, seq - fresh_j * a.page_size, a.num_kv_heads,
+                                            a.page_size);
+        __syncwarp();
+    }
+    float *srow = a.scores + int64_t(row) * a.max_pages;
+    if (w_page0 >= n_b || (a.top_k >= n_b && !score_all)) return;
+
     uint4 av[4][NKP];
-    bound_load_meta<D, HINT>(a, r.g, pp, vv, bad, av, HINT ? l2_evict_first_policy() : 0, jj, fresh_j);
-    bound_score_store<D, QF32>(a, qraw, av, jj, vv, bad, w_page0, r.n_b, srow);
+    bound_load_meta<D, HINT>(a, g, pp, vv, bad, av, HINT ? l2_evict_first_policy() : 0, jj, fresh_j);
+    bound_score_store<D, QF32>(a, qraw, av, jj, vv, bad, w_page0, n_b, srow);
 }
 
 // -------------------------------------------------- scores on CUDA cores --
