@@ -690,7 +690,8 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
     """The library's launches in one step: metadata refresh (inside the
     scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
     (sparse only), decode, and the merge kernel unless the decode grid folds
-    its split rows itself (bf16 KV, no shared prefix, and a row's pieces fit
+    its split rows itself (one row per CTA when the rows fit one wave of
+    decode CTAs at d = 128, or) (bf16 KV, no shared prefix, and a row's pieces fit
     one warp's single round of loads: pieces x G x d / 128 <= 16, with the
     grid's 2 CTAs x 6 warps per SM); a cascade adds the prefix kernel."""
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
@@ -698,8 +699,10 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
     spr = spec.top_k if spec.top_k is not None else inputs["page_table"].shape[1] - prefix
     upw = max(1, -(-rows * spr // (2 * sms * 6)))
     pieces = -(-spr // upw) + 1
-    fold = (spec.kv_dtype == torch.bfloat16 and prefix == 0
-            and pieces * max(1, spec.group * spec.head_dim // 128) <= 16)
+    row_per_cta = (spec.kv_dtype == torch.bfloat16 and prefix == 0 and spec.head_dim == 128
+                   and sms <= rows <= 2 * sms and spr <= 1024)
+    fold = row_per_cta or (spec.kv_dtype == torch.bfloat16 and prefix == 0
+                           and pieces * max(1, spec.group * spec.head_dim // 128) <= 16)
     # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV
     fused_refresh = spec.kv_dtype == torch.bfloat16 and scorer == "bound" and not approx
     n = ((2 if fused_refresh else 3) if spec.top_k is not None else 0) + 1 + (0 if fold else 1)

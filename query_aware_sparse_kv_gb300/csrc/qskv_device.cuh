@@ -573,6 +573,9 @@ constexpr int kDecodeWarpsD128 = QSKV_D128_WARPS, kDecodeHalvesD128 = QSKV_D128_
 constexpr int kDecodeWarpsD64 = QSKV_D64_WARPS, kDecodeHalvesD64 = QSKV_D64_HALVES,
               kDecodeStagesD64 = QSKV_D64_STAGES;
 constexpr int kMaxStages = 8;
+// Most units a row may have for the one-row-per-CTA decode (their codes sit
+// in shared memory beside the rings).
+constexpr int kRowCtaMaxSlots = 1024;
 // The decode grid folds a split row itself when one warp can load all of the
 // row's pieces in a single round of at most this many 16-byte loads per lane
 // (pieces x G x D / 128).  Measured on GB300: the GPT2-like rows (15 pieces
