@@ -689,18 +689,24 @@ class Bench:
 def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bound", approx: bool = False) -> int:
     """The library's launches in one step: metadata refresh (inside the
     scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
-    (sparse only), decode, and the merge kernel unless the decode grid folds
-    its split rows itself (one row per CTA when the rows fit one wave of
-    decode CTAs at d = 128, or) (bf16 KV, no shared prefix, and a row's pieces fit
-    one warp's single round of loads: pieces x G x d / 128 <= 16, with the
-    grid's 2 CTAs x 6 warps per SM); a cascade adds the prefix kernel."""
+    (sparse only), decode, and the merge kernel unless the decode folds the
+    rows' pieces itself: bf16 KV without a shared prefix, and either the rows
+    fit one wave of decode CTAs (one row per k CTAs: k = 1 for one or two rows
+    per SM, else min(2 SMs / rows, 8, units / 4) when that gives every SM a
+    CTA) or a row's stream-K pieces fit one warp's single round of loads
+    (pieces x G x d / 128 <= 16, with the grid's 2 CTAs x 6 warps per SM); a
+    cascade adds the prefix kernel."""
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     rows = spec.batch * spec.num_kv_heads
     spr = spec.top_k if spec.top_k is not None else inputs["page_table"].shape[1] - prefix
     upw = max(1, -(-rows * spr // (2 * sms * 6)))
     pieces = -(-spr // upw) + 1
-    row_per_cta = (spec.kv_dtype == torch.bfloat16 and prefix == 0 and spec.head_dim == 128
-                   and sms <= rows <= 2 * sms and spr <= 1024)
+    ctas = 2 * sms
+    k = 0
+    if spec.kv_dtype == torch.bfloat16 and prefix == 0 and 0 < rows <= ctas and spr <= 1024:
+        k = 1 if rows >= sms else min(ctas // rows, 8, spr // 4)
+        k = k if k == 1 or (k >= 2 and rows * k >= sms) else 0
+    row_per_cta = k > 0
     fold = row_per_cta or (spec.kv_dtype == torch.bfloat16 and prefix == 0
                            and pieces * max(1, spec.group * spec.head_dim // 128) <= 16)
     # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV

@@ -229,13 +229,18 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // then V, each half as D/64 boxes of 16 tokens x 64 dims (128-byte swizzle).
 // HINT: the call streams more K/V than L2 holds; the loads carry an
 // evict-first L2 policy.
-// ROWCTA: CTA r decodes row r alone (used when the rows fit one wave of
-// CTAs).  The CTA first reads the row's unit codes into shared memory; warp w
-// then takes units w, w + WPC, w + 2 WPC, ... (a fixed split, so repeated
-// calls give bit-identical results; a shared counter handing units out in
-// arrival order measured 1.3 % faster and is not deterministic).  Each warp
-// leaves its piece in its own ring and, after a CTA barrier, the CTA folds
-// the pieces into the row's output: no global partials, no merge kernel.
+// ROWCTA: the row_blocks (k <= kRowBlocksMax) CTAs c = k r .. k r + k - 1 decode row r alone
+// (used when the rows fit one wave of CTAs: k = 1 with one or two rows per
+// SM, k > 1 with fewer rows than SMs).  A CTA first reads the row's unit
+// codes into shared memory; warp w of block j then takes units j + k (w + WPC
+// n), n = 0, 1, ... (a fixed split, so repeated calls give bit-identical
+// results; with k = 1 a shared counter handing units out in arrival order
+// measured 1.3 % faster and is not deterministic).  Each warp leaves its
+// piece in its own ring and, after a CTA barrier, the CTA folds the pieces:
+// with k = 1 into the row's output (no global partials, no merge kernel);
+// with k > 1 into one piece per block in the workspace, and the block that
+// draws the row's last ticket (a per-row counter; no block waits for
+// another) folds the k pieces with all its threads and resets the counter.
 template <int D, bool QF32, int WPC, int HALVES, bool HINT, bool ROWCTA>
 __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -257,7 +262,9 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     const int S = a.stages;
     const int G = a.group;
     const int64_t gw = int64_t(blockIdx.x) * WPC + warp;
-    const int64_t u_begin = ROWCTA ? int64_t(blockIdx.x) * a.slots_per_row : gw * a.units_per_warp;
+    const int rc_k = ROWCTA ? a.row_blocks : 1;
+    const int rc_row = ROWCTA ? int(blockIdx.x) / rc_k : 0, rc_blk = ROWCTA ? int(blockIdx.x) % rc_k : 0;
+    const int64_t u_begin = ROWCTA ? int64_t(rc_row) * a.slots_per_row : gw * a.units_per_warp;
     const int64_t u_end = ROWCTA ? u_begin + a.slots_per_row : min(u_begin + a.units_per_warp, a.total_units);
     pdl_trigger();
     if (!ROWCTA && u_begin >= u_end) {
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     __syncwarp();
     if (!a.wait_at_exit) pdl_wait();
     if constexpr (ROWCTA) {
-        for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32) s_code[i] = unit_code(a, blockIdx.x, i);
+        for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32) s_code[i] = unit_code(a, rc_row, i);
         __syncthreads();
     }
     // K/V streams larger than L2 are read evict-first; smaller ones with no
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             if constexpr (ROWCTA) {
                 while (nh < HALVES && !rc_done) {
                     if (psub == 0) {  // the warp's next unit: slots warp, warp + WPC, ...
-                        const int idx = rc_taken * WPC + warp;
+                        const int idx = rc_blk + rc_k * (rc_taken * WPC + warp);
                         rc_taken++;
                         if (idx >= spr) {
                             rc_done = true;
@@ -696,8 +703,9 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         }
         __syncthreads();
         // out = sum_w 2^(lse_w - m) o_w / sum_w 2^(lse_w - m), m = max_w lse_w
-        const int row = blockIdx.x, b = row / a.num_kv_heads, g = row % a.num_kv_heads;
+        const int row = rc_row, b = row / a.num_kv_heads, g = row % a.num_kv_heads;
         const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
+        const int64_t slot = int64_t(row) * rc_k + rc_blk;  // k > 1: this block's piece
         for (int e = threadIdx.x; e < G * D; e += WPC * 32) {
             const int h = e / D;
             float m = -INFINITY;
@@ -716,9 +724,63 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                     acc = fmaf(wt, pw[e], acc);
                 }
             }
-            a.out[qh0 * D + e] = den > 0.f ? acc / den : 0.f;
-            if (a.lse && e % D == 0) a.lse[qh0 + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+            if (rc_k == 1) {
+                a.out[qh0 * D + e] = den > 0.f ? acc / den : 0.f;
+                if (a.lse && e % D == 0) a.lse[qh0 + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+            } else {
+                a.part_o[slot * G * D + e] = den > 0.f ? acc / den : 0.f;
+                if (e % D == 0) a.part_lse[slot * G + h] = den > 0.f ? m + log2f(den) : -INFINITY;
+            }
         }
+        if (rc_k == 1) return;
+        // k > 1: the block drawing the row's last ticket folds the k pieces
+        __shared__ uint32_t s_last;
+        __threadfence();  // this thread's piece stores, before the ticket
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            s_last = atomicAdd(a.tickets + row, 1u) == uint32_t(rc_k - 1) ? 1u : 0u;
+            if (s_last) __threadfence();  // the other blocks' pieces, before they are read
+        }
+        __syncthreads();
+        if (!s_last) return;
+        // the k x G log-sum-exps into shared memory, then per float4 column
+        // the k pieces' loads issued together (one round for G x D <= 768)
+        __shared__ float s_plse[kRowBlocksMax * 8];
+        const int64_t s0 = int64_t(row) * rc_k;
+        for (int i = threadIdx.x; i < rc_k * G; i += WPC * 32) s_plse[i] = __ldcg(a.part_lse + s0 * G + i);
+        constexpr int V4 = D / 4;
+        __syncthreads();
+        for (int c = threadIdx.x; c < G * V4; c += WPC * 32) {
+            const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + s0 * G * V4 + c;
+            float4 v[kRowBlocksMax];
+#pragma unroll
+            for (int j = 0; j < kRowBlocksMax; j++)
+                v[j] = j < rc_k ? __ldcg(po + int64_t(j) * G * V4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int h = c / V4;
+            float m = -INFINITY;
+            for (int j = 0; j < rc_k; j++) m = fmaxf(m, s_plse[j * G + h]);
+            float den = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int j = 0; j < kRowBlocksMax; j++) {
+                    if (j >= rc_k) break;
+                    const float l = s_plse[j * G + h];
+                    if (l == -INFINITY) continue;  // an empty piece: its o holds no data
+                    const float wt = exp2f(l - m);
+                    den += wt;
+                    acc.x = fmaf(wt, v[j].x, acc.x);
+                    acc.y = fmaf(wt, v[j].y, acc.y);
+                    acc.z = fmaf(wt, v[j].z, acc.z);
+                    acc.w = fmaf(wt, v[j].w, acc.w);
+                }
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            reinterpret_cast<float4 *>(a.out + qh0 * D)[c] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (a.lse && c % V4 == 0) a.lse[qh0 + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+        }
+        if (threadIdx.x == 0) a.tickets[row] = 0u;
         return;
     }
     if (cur_row >= 0) finish_row(cur_row);
@@ -834,7 +896,7 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     if (grid.warps_per_cta != WPC) return cudaErrorInvalidConfiguration;
     // ROWCTA: one CTA per row, the row's unit codes after the rings
     const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? size_t(a.slots_per_row) * 4 : 0);
-    const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads) : unsigned(grid.ctas);
+    const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads * a.row_blocks) : unsigned(grid.ctas);
     auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
     static std::mutex mu;                // calls may come from several host threads
@@ -854,11 +916,9 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
 template <int D, bool QF32>
 cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
                         cudaStream_t stream, bool rowcta = false) {
-    if constexpr (D == 128) {
-        if (rowcta)
-            return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true>(a, tk, tv, grid, stream)
-                                    : launch_bf16_hint<D, QF32, false, true>(a, tk, tv, grid, stream);
-    }
+    if (rowcta)
+        return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true>(a, tk, tv, grid, stream)
+                                : launch_bf16_hint<D, QF32, false, true>(a, tk, tv, grid, stream);
     return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, false>(a, tk, tv, grid, stream)
                             : launch_bf16_hint<D, QF32, false, false>(a, tk, tv, grid, stream);
 }
@@ -887,6 +947,17 @@ cudaError_t noalloc_scratch_address(void **ptr) {
     }
     *ptr = addr[dev];
     return cudaSuccess;
+}
+
+int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_pieces, bool have_tickets) {
+    if (!no_extra_pieces || rows <= 0 || rows > ctas || slots_per_row > kRowCtaMaxSlots) return 0;
+    const int64_t sms = ctas / kDecodeCtasPerSm;
+    if (rows >= sms) return 1;
+    if (!have_tickets) return 0;
+    int64_t k = ctas / rows;
+    k = k < kRowBlocksMax ? k : kRowBlocksMax;
+    k = k < slots_per_row / 4 ? k : slots_per_row / 4;
+    return k >= 2 && rows * k >= sms ? int(k) : 0;
 }
 
 int decode_stages(int head_dim) { return head_dim == 128 ? kDecodeStagesD128 : kDecodeStagesD64; }
@@ -940,22 +1011,23 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
     }
     if (a.total_units == 0) return cudaSuccess;
     if (kv_dtype == kDtypeBf16) {
-        // Rows that fit one wave of CTAs (at least one per SM, at most
-        // kDecodeCtasPerSm per SM) are decoded one row per CTA, the pieces
-        // folded in the CTA: no merge kernel (d = 128).
-        const int64_t rows = int64_t(a.batch) * a.num_kv_heads;
-        const int64_t sms = grid.ctas / kDecodeCtasPerSm;
-        if (head_dim == 128 && a.extra_pieces == 0 && rows >= sms && rows <= grid.ctas &&
-            a.slots_per_row <= kRowCtaMaxSlots) {
+        // Rows that fit one wave of CTAs are decoded one row per k CTAs (the
+        // pieces folded in the CTA, then across the k CTAs by the last one):
+        // k = 1 with one or two rows per SM, k > 1 with fewer rows than SMs
+        // (up to kRowBlocksMax, at least 4 units per CTA, and then at least
+        // one CTA per SM; the fold across CTAs needs the per-row counters).
+        const int k = row_blocks_for(int64_t(a.batch) * a.num_kv_heads, a.slots_per_row, grid.ctas,
+                                     a.extra_pieces == 0, a.tickets != nullptr);
+        if (k > 0) {
             DecodeArgs d = da;
             d.fold = 0;
-            return qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream, true)
-                      : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream, true);
+            d.row_blocks = k;
+            if (head_dim == 128)
+                return qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream, true)
+                          : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream, true);
+            return qf ? launch_bf16<64, true>(d, tmap_k, tmap_v, grid, stream, true)
+                      : launch_bf16<64, false>(d, tmap_k, tmap_v, grid, stream, true);
         }
-        // A split row is folded inside the decode grid by its last warp when
-        // that warp can fetch all the row's pieces in one round of loads (at
-        // most kFoldMaxLoads 16-byte loads per lane); otherwise the merge
-        // kernel, with a CTA per row, folds it.
         const int64_t upw = a.units_per_warp > 0 ? a.units_per_warp : 1;
         const int64_t pieces = (a.slots_per_row + upw - 1) / upw + 1;
         const int64_t per_lane = a.group * head_dim / 128 > 1 ? a.group * head_dim / 128 : 1;

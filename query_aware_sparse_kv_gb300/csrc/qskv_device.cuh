@@ -498,6 +498,7 @@ struct DecodeArgs {
     int64_t total_units;    // rows * slots_per_row
     int64_t units_per_warp; // ceil(total_units / total_warps)
     float scale_log2;       // sm_scale * log2(e)
+    int32_t row_blocks = 1; // one-row-per-CTA decode: CTAs per row (1: the CTA finishes the row)
 };
 
 // Shared-prefix cascade: the attention of all B x G query rows of one KV head
@@ -574,8 +575,10 @@ constexpr int kDecodeWarpsD64 = QSKV_D64_WARPS, kDecodeHalvesD64 = QSKV_D64_HALV
               kDecodeStagesD64 = QSKV_D64_STAGES;
 constexpr int kMaxStages = 8;
 // Most units a row may have for the one-row-per-CTA decode (their codes sit
-// in shared memory beside the rings).
+// in shared memory beside the rings), and the most CTAs it splits a row over
+// (their pieces are folded with one round of loads).
 constexpr int kRowCtaMaxSlots = 1024;
+constexpr int kRowBlocksMax = 8;
 // The decode grid folds a split row itself when one warp can load all of the
 // row's pieces in a single round of at most this many 16-byte loads per lane
 // (pieces x G x D / 128).  Measured on GB300: the GPT2-like rows (15 pieces

@@ -74,6 +74,11 @@ cudaError_t launch_prefix(const PrefixArgs &a, const CUtensorMap *tmap_k, const 
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
 cudaError_t noalloc_scratch_address(void **ptr);
 
+// CTAs per row of the one-row-per-CTA decode for `rows` rows of
+// slots_per_row units on a grid of `ctas` CTA slots (0: use the stream-K
+// split instead).
+int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_pieces, bool have_tickets);
+
 // Stage count and dynamic shared memory of the bf16 decode kernel.
 int decode_stages(int head_dim);
 int decode_warps_per_cta(int head_dim);

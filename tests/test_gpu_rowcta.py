@@ -1,13 +1,15 @@
-"""One row per decode CTA.
+"""One row per k decode CTAs.
 
-When the (sequence, KV head) rows fit one wave of decode CTAs (at least one
-and at most two per SM, d = 128, bf16 KV), CTA r decodes row r alone: its
-warps take the row's selected pages from a shared-memory counter and the
-warps' partial results are folded in the CTA by log-sum-exp rescaling
-(Quail AI-SQL engine article: partial attention combined as in flash
-decoding), with no merge kernel.  Sparse rows -- some with fewer pages than
-top_k -- and a dense batch are checked row by row against the oracle, and
-repeated calls on one workspace give identical results."""
+When the (sequence, KV head) rows fit one wave of decode CTAs (bf16 KV), the
+k CTAs of row r decode it alone: each CTA's warps take a fixed share of the
+row's selected pages and fold their partial results in the CTA by
+log-sum-exp rescaling (Quail AI-SQL engine article: partial attention
+combined as in flash decoding); with k = 1 (one or two rows per SM) that is
+the row's output, with k > 1 (fewer rows than SMs) the CTA drawing the row's
+last ticket folds the k pieces.  No merge kernel either way.  Sparse rows --
+some with fewer pages than top_k -- and dense batches, d = 128 and d = 64,
+are checked row by row against the oracle, and repeated calls on one
+workspace give identical results."""
 import pytest
 import torch
 
@@ -31,8 +33,26 @@ def _sms():
     return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
+def row_blocks(rows, slots, sms):
+    """CTAs per row the library picks (0: the stream-K split)."""
+    ctas = 2 * sms
+    if rows <= 0 or rows > ctas or slots > 1024:
+        return 0
+    if rows >= sms:
+        return 1
+    k = min(ctas // rows, 8, slots // 4)
+    return k if k >= 2 and rows * k >= sms else 0
+
+
 def _case(kind):
     sms = _sms()
+    if kind == "blocks_gpt2":   # 128 MHA rows, d = 64, fp32 q: two CTAs per row
+        return W.spec_for("gpt2_345m")
+    if kind == "blocks_long":   # 24 rows of 32-token pages: eight CTAs per row
+        return W.spec_for("long_context", batch=3, seq_len_range=(3000, 9000), max_pages=None, top_k=64)
+    if kind == "blocks_dense":  # dense d = 64 rows, fewer rows than SMs
+        return W.spec_for("gpt2_345m", batch=7, seq_lens=None, seq_len_range=(400, 1500), max_pages=None, top_k=None,
+                          num_q_heads=16, num_kv_heads=16)
     if kind == "sparse_mid":    # about 1.3 rows per SM, lengths around top_k
         return W.spec_for("llama3_8b", batch=(4 * sms) // (3 * 8), seq_len_range=(200, 6000), max_pages=None)
     if kind == "sparse_low":    # one row per SM (the smallest row count of the mode)
@@ -43,12 +63,18 @@ def _case(kind):
                       top_k=None)
 
 
-@pytest.mark.parametrize("kind", ["sparse_mid", "sparse_low", "sparse_high", "dense"])
+@pytest.mark.parametrize("kind", ["sparse_mid", "sparse_low", "sparse_high", "dense", "blocks_gpt2", "blocks_long",
+                                  "blocks_dense"])
 def test_row_per_cta_matches_the_oracle(oracle_lib, kind):
     spec = _case(kind)
     rows = spec.batch * spec.num_kv_heads
-    assert _sms() <= rows <= 2 * _sms(), "the case must fall in the one-row-per-CTA range"
     inp = W.make_inputs(spec)
+    slots = spec.top_k if spec.top_k is not None else inp["page_table"].shape[1]
+    k = row_blocks(rows, slots, _sms())
+    if kind.startswith("blocks"):
+        assert k > 1, f"the case must split its rows over several CTAs (k = {k})"
+    else:
+        assert k == 1, f"the case must give each row one CTA (k = {k})"
     dec = qskv.from_inputs(inp)
     dense = spec.top_k is None
     o_meta = None
