@@ -52,7 +52,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // (physical page << 6 | valid tokens) of slot `slot` of row `row`, or -1
 // when the slot is empty or names an out-of-range page (flagged).  The
 // index loads that do not depend on each other are issued together.
-__device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot) {
+// pt_row: the sequence's page-table row (global memory, or a copy in shared
+// memory).
+__device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot, const int32_t *pt_row = nullptr) {
     const int b = row / a.num_kv_heads;
     int seq = __ldg(a.seq_lens + b);
     int ns = 0, j = slot + a.page_begin;
@@ -80,7 +82,7 @@ __device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot)
     } else if (j >= n_b) {
         return -1;
     }
-    const int p = __ldg(a.page_table + int64_t(b) * a.max_pages + j);
+    const int p = pt_row ? pt_row[j] : __ldg(a.page_table + int64_t(b) * a.max_pages + j);
     if (p < 0 || p >= a.num_pool_pages) {
         raise_error(a.flags, kErrPageId);
         return -1;
@@ -275,6 +277,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     uint8_t *ring0 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = ring0 + size_t(warp) * S * STAGE;
     int *s_code = reinterpret_cast<int *>(ring0 + size_t(WPC) * S * STAGE);  // ROWCTA: [slots_per_row]
+    int32_t *s_pt = s_code + ((a.slots_per_row + 3) & ~3);                   // ROWCTA: [max_pages] if staged
     uint64_t *bar = bars[warp];
     if (lane == 0) {
         for (int s = 0; s < S; s++) mbar_init(bar + s, 1);
@@ -283,9 +286,21 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         prefetch_tensormap(&tmap_v);
     }
     __syncwarp();
+    if constexpr (ROWCTA) {
+        // The page table is an input no kernel of this library writes, so the
+        // row's entries are staged before the wait for the previous kernel
+        // (which ends the selection), leaving one dependent round trip
+        // (selected -> code) after it.
+        if (a.pt_in_smem) {
+            const int32_t *pt = a.page_table + int64_t(rc_row / a.num_kv_heads) * a.max_pages;
+            for (int j = threadIdx.x; j < a.max_pages; j += WPC * 32) s_pt[j] = __ldg(pt + j);
+        }
+    }
     if (!a.wait_at_exit) pdl_wait();
     if constexpr (ROWCTA) {
-        for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32) s_code[i] = unit_code(a, rc_row, i);
+        __syncthreads();
+        for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
+            s_code[i] = unit_code(a, rc_row, i, a.pt_in_smem ? s_pt : nullptr);
         __syncthreads();
     }
     // K/V streams larger than L2 are read evict-first; smaller ones with no
@@ -894,8 +909,8 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     constexpr int WPC = D == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64;
     constexpr int HALVES = D == 128 ? kDecodeHalvesD128 : kDecodeHalvesD64;
     if (grid.warps_per_cta != WPC) return cudaErrorInvalidConfiguration;
-    // ROWCTA: one CTA per row, the row's unit codes after the rings
-    const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? size_t(a.slots_per_row) * 4 : 0);
+    // ROWCTA: the row's unit codes after the rings, then its page-table row if staged
+    const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? rowcta_extra_smem(a) : 0);
     const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads * a.row_blocks) : unsigned(grid.ctas);
     auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
@@ -949,6 +964,10 @@ cudaError_t noalloc_scratch_address(void **ptr) {
     return cudaSuccess;
 }
 
+size_t rowcta_extra_smem(const DecodeArgs &a) {
+    return size_t((a.slots_per_row + 3) & ~3) * 4 + (a.pt_in_smem ? size_t(a.max_pages) * 4 : 0);
+}
+
 int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_pieces, bool have_tickets) {
     if (!no_extra_pieces || rows <= 0 || rows > ctas || slots_per_row > kRowCtaMaxSlots) return 0;
     const int64_t sms = ctas / kDecodeCtasPerSm;
@@ -958,6 +977,25 @@ int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_piec
     k = k < kRowBlocksMax ? k : kRowBlocksMax;
     k = k < slots_per_row / 4 ? k : slots_per_row / 4;
     return k >= 2 && rows * k >= sms ? int(k) : 0;
+}
+
+size_t rowcta_smem_budget() {
+    // dynamic shared memory per CTA with kDecodeCtasPerSm CTAs per SM (less
+    // a margin for the kernel's static shared memory), cached per device
+    static size_t budget[64] = {0};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!budget[dev]) {
+        int per_sm = 0, reserved = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            return 0;
+        const int64_t b = int64_t(per_sm) / kDecodeCtasPerSm - reserved - 2048;
+        budget[dev] = b > 0 ? size_t(b) : 1;
+    }
+    return budget[dev];
 }
 
 int decode_stages(int head_dim) { return head_dim == 128 ? kDecodeStagesD128 : kDecodeStagesD64; }
@@ -1022,6 +1060,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
             DecodeArgs d = da;
             d.fold = 0;
             d.row_blocks = k;
+            // stage the page-table row when two CTAs per SM still fit
+            d.pt_in_smem = 1;
+            const size_t need = decode_smem_bytes(head_dim, d.stages) + rowcta_extra_smem(d);
+            if (need > rowcta_smem_budget()) d.pt_in_smem = 0;
             if (head_dim == 128)
                 return qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream, true)
                           : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream, true);

@@ -499,6 +499,8 @@ struct DecodeArgs {
     int64_t units_per_warp; // ceil(total_units / total_warps)
     float scale_log2;       // sm_scale * log2(e)
     int32_t row_blocks = 1; // one-row-per-CTA decode: CTAs per row (1: the CTA finishes the row)
+    int32_t pt_in_smem = 0; // one-row-per-CTA decode: the row's page-table entries are staged in
+                            // shared memory before the wait for the previous kernel
 };
 
 // Shared-prefix cascade: the attention of all B x G query rows of one KV head
