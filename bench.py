@@ -656,8 +656,9 @@ class Bench:
 
     def e2e(self, steps: int, warmup: int, world: int, zero_copy: bool) -> float:
         """Steps/s through the public API: one graph per step recorded by
-        PagedDecoder.capture_step with pinned host q / out (the kernels read q
-        from and write out to host memory when zero_copy), the host waiting
+        PagedDecoder.capture_step with pinned host q / out (a copy node brings
+        q in; the decode writes out to host memory when zero_copy, else a copy
+        node takes it out), the host waiting
         for every step's output (PagedDecoder.wait)."""
         dec, spec = self.dec, self.spec
         q_host = self.qv_cpu.pin_memory()
@@ -852,8 +853,9 @@ def run_gpu(args):
                         "CUDA graph replay, one graph per query variant (dense decode: no metadata refresh or selection)"),
         "eager_ms_per_step": eager_ms,
         "e2e": {"value": e2e_value, "unit": "steps/s", "steps": e2e_steps,
-                "path": "PagedDecoder.capture_step(q_host, out_host) replay: kernels read q from and write out to "
-                        "pinned host memory (zero-copy), host waits for every step (PagedDecoder.wait)",
+                "path": "PagedDecoder.capture_step(q_host, out_host) replay: a copy node brings q in from pinned "
+                        "host memory, the decode writes out straight to pinned host memory (zero-copy), host "
+                        "waits for every step (PagedDecoder.wait)",
                 "copy_nodes_value": e2e_copy_nodes,
                 "h2d_bytes_per_step": getattr(main, "e2e_h2d", 0), "d2h_bytes_per_step": getattr(main, "e2e_d2h", 0)},
         # kernels per step: metadata refresh (fused into scoring where it can be), scoring, ranking,

@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     uint8_t *ring = ring0 + size_t(warp) * S * STAGE;
     int *s_code = reinterpret_cast<int *>(ring0 + size_t(WPC) * S * STAGE);  // ROWCTA: [slots_per_row]
     int32_t *s_pt = s_code + ((a.slots_per_row + 3) & ~3);                   // ROWCTA: [max_pages] if staged
+    uint4 *s_q = reinterpret_cast<uint4 *>(s_pt + (a.pt_in_smem ? ((a.max_pages + 3) & ~3) : 0));  // ROWCTA: [G][D]
     uint64_t *bar = bars[warp];
     if (lane == 0) {
         for (int s = 0; s < S; s++) mbar_init(bar + s, 1);
@@ -295,6 +296,13 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             const int32_t *pt = a.page_table + int64_t(rc_row / a.num_kv_heads) * a.max_pages;
             for (int j = threadIdx.x; j < a.max_pages; j += WPC * 32) s_pt[j] = __ldg(pt + j);
         }
+        // the group's G query rows (contiguous), once per CTA in 16-byte
+        // vectors (q may sit in host memory: few, whole-line requests)
+        constexpr int QV = D * (QF32 ? 4 : 2) / 16;  // uint4 per query row
+        const uint4 *qg = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(a.q) +
+                          (int64_t(rc_row / a.num_kv_heads) * a.num_q_heads + int64_t(rc_row % a.num_kv_heads) * G) *
+                              D * (QF32 ? 4 : 2));
+        for (int i = threadIdx.x; i < G * QV; i += WPC * 32) s_q[i] = qg[i];
     }
     if (!a.wait_at_exit) pdl_wait();
     if constexpr (ROWCTA) {
@@ -456,12 +464,15 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
 #pragma unroll
         for (int i = 0; i < NKS; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         const bool ok = gid < G;
-        const int64_t qoff = (int64_t(b) * a.num_q_heads + int64_t(g) * G + (ok ? gid : 0)) * D;
+        // ROWCTA: the group's queries were staged in shared memory (s_q)
+        const void *qbase = ROWCTA ? static_cast<const void *>(s_q) : a.q;
+        const int64_t qoff = ROWCTA ? int64_t(ok ? gid : 0) * D
+                                    : (int64_t(b) * a.num_q_heads + int64_t(g) * G + (ok ? gid : 0)) * D;
 #pragma unroll
         for (int ks = 0; ks < NKS; ks++) {
             const int k0 = ks * 16 + 2 * t;
             if (QF32) {
-                const float *q = static_cast<const float *>(a.q) + qoff;
+                const float *q = static_cast<const float *>(qbase) + qoff;
                 const float2 x0 = *reinterpret_cast<const float2 *>(q + k0);
                 const float2 x1 = *reinterpret_cast<const float2 *>(q + k0 + 8);
                 const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                 ql[ks][0] = ok ? pack_bf16x2(x0.x - bf16_lo_to_float(h0), x0.y - bf16_hi_to_float(h0)) : 0u;
                 ql[ks][1] = ok ? pack_bf16x2(x1.x - bf16_lo_to_float(h1), x1.y - bf16_hi_to_float(h1)) : 0u;
             } else {
-                const uint32_t *q = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(a.q) + qoff);
+                const uint32_t *q = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(qbase) + qoff);
                 qb[ks][0] = ok ? q[k0 / 2] : 0u;
                 qb[ks][1] = ok ? q[(k0 + 8) / 2] : 0u;
             }
@@ -721,13 +732,15 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         const int row = rc_row, b = row / a.num_kv_heads, g = row % a.num_kv_heads;
         const int64_t qh0 = int64_t(b) * a.num_q_heads + int64_t(g) * G;
         const int64_t slot = int64_t(row) * rc_k + rc_blk;  // k > 1: this block's piece
-        for (int e = threadIdx.x; e < G * D; e += WPC * 32) {
-            const int h = e / D;
+        constexpr int V4 = D / 4;
+        for (int c = threadIdx.x; c < G * V4; c += WPC * 32) {  // float4 columns (vector stores)
+            const int h = c / V4;
             float m = -INFINITY;
 #pragma unroll
             for (int w = 0; w < WPC; w++)
                 m = fmaxf(m, reinterpret_cast<const float *>(ring0 + size_t(w) * S * STAGE)[G * D + h]);
-            float den = 0.f, acc = 0.f;
+            float den = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (m != -INFINITY) {
 #pragma unroll
                 for (int w = 0; w < WPC; w++) {
@@ -735,16 +748,22 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                     const float l = pw[G * D + h];
                     if (l == -INFINITY) continue;  // a warp without units: no data
                     const float wt = exp2f(l - m);
+                    const float4 v = reinterpret_cast<const float4 *>(pw)[c];
                     den += wt;
-                    acc = fmaf(wt, pw[e], acc);
+                    acc.x = fmaf(wt, v.x, acc.x);
+                    acc.y = fmaf(wt, v.y, acc.y);
+                    acc.z = fmaf(wt, v.z, acc.z);
+                    acc.w = fmaf(wt, v.w, acc.w);
                 }
             }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            const float4 r4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             if (rc_k == 1) {
-                a.out[qh0 * D + e] = den > 0.f ? acc / den : 0.f;
-                if (a.lse && e % D == 0) a.lse[qh0 + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+                reinterpret_cast<float4 *>(a.out + qh0 * D)[c] = r4;
+                if (a.lse && c % V4 == 0) a.lse[qh0 + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
             } else {
-                a.part_o[slot * G * D + e] = den > 0.f ? acc / den : 0.f;
-                if (e % D == 0) a.part_lse[slot * G + h] = den > 0.f ? m + log2f(den) : -INFINITY;
+                reinterpret_cast<float4 *>(a.part_o + slot * G * D)[c] = r4;
+                if (c % V4 == 0) a.part_lse[slot * G + h] = den > 0.f ? m + log2f(den) : -INFINITY;
             }
         }
         if (rc_k == 1) return;
@@ -763,7 +782,6 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
         __shared__ float s_plse[kRowBlocksMax * 8];
         const int64_t s0 = int64_t(row) * rc_k;
         for (int i = threadIdx.x; i < rc_k * G; i += WPC * 32) s_plse[i] = __ldcg(a.part_lse + s0 * G + i);
-        constexpr int V4 = D / 4;
         __syncthreads();
         for (int c = threadIdx.x; c < G * V4; c += WPC * 32) {
             const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + s0 * G * V4 + c;
@@ -910,7 +928,7 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     constexpr int HALVES = D == 128 ? kDecodeHalvesD128 : kDecodeHalvesD64;
     if (grid.warps_per_cta != WPC) return cudaErrorInvalidConfiguration;
     // ROWCTA: the row's unit codes after the rings, then its page-table row if staged
-    const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? rowcta_extra_smem(a) : 0);
+    const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? rowcta_extra_smem(a, D * (QF32 ? 4 : 2)) : 0);
     const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads * a.row_blocks) : unsigned(grid.ctas);
     auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
@@ -964,8 +982,9 @@ cudaError_t noalloc_scratch_address(void **ptr) {
     return cudaSuccess;
 }
 
-size_t rowcta_extra_smem(const DecodeArgs &a) {
-    return size_t((a.slots_per_row + 3) & ~3) * 4 + (a.pt_in_smem ? size_t(a.max_pages) * 4 : 0);
+size_t rowcta_extra_smem(const DecodeArgs &a, int q_bytes) {
+    return size_t((a.slots_per_row + 3) & ~3) * 4 + (a.pt_in_smem ? size_t((a.max_pages + 3) & ~3) * 4 : 0) +
+           size_t(a.group) * q_bytes;
 }
 
 int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_pieces, bool have_tickets) {
@@ -1062,7 +1081,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
             d.row_blocks = k;
             // stage the page-table row when two CTAs per SM still fit
             d.pt_in_smem = 1;
-            const size_t need = decode_smem_bytes(head_dim, d.stages) + rowcta_extra_smem(d);
+            const size_t need = decode_smem_bytes(head_dim, d.stages) + rowcta_extra_smem(d, head_dim * (qf ? 4 : 2));
             if (need > rowcta_smem_budget()) d.pt_in_smem = 0;
             if (head_dim == 128)
                 return qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream, true)

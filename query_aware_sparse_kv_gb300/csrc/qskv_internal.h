@@ -79,9 +79,10 @@ cudaError_t noalloc_scratch_address(void **ptr);
 // split instead).
 int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_pieces, bool have_tickets);
 // Shared memory the one-row-per-CTA decode needs beyond the rings (the unit
-// codes, and the page-table row when a.pt_in_smem), and the dynamic shared
-// memory a decode CTA may take with two CTAs per SM on the current device.
-size_t rowcta_extra_smem(const DecodeArgs &a);
+// codes, the page-table row when a.pt_in_smem, the group's queries of
+// q_bytes each), and the dynamic shared memory a decode CTA may take with
+// two CTAs per SM on the current device.
+size_t rowcta_extra_smem(const DecodeArgs &a, int q_bytes);
 size_t rowcta_smem_budget();
 
 // Stage count and dynamic shared memory of the bf16 decode kernel.

@@ -142,20 +142,20 @@ class PagedDecoder:
         With pinned host tensors ``q_host`` (shaped like q) and/or
         ``out_host`` (shaped like out) the graph also moves the query in and
         the output out, so a serving loop launches one graph per step and
-        synchronises once.  zero_copy=True (default): the kernels read the
-        query straight from ``q_host`` and write the output straight into
+        synchronises once: a copy node brings ``q_host`` into ``q`` first
+        (the scoring grid reads the query once per page chunk, so it is read
+        from device memory), refill ``q_host`` before each replay.
+        zero_copy=True (default): the decode writes the output straight into
         ``out_host`` (pinned host memory is device-accessible; on GB300 the
-        NVLink-C2C link makes this faster than copy nodes); refill ``q_host``
-        before each replay, and ``out`` is not written.  zero_copy=False: copy
-        nodes from ``q_host`` into ``q`` first and from ``out`` into
+        NVLink-C2C link makes this faster than a copy node), and ``out`` is
+        not written.  zero_copy=False: a copy node from ``out`` into
         ``out_host`` last."""
         def body():
-            if zero_copy:
-                self.step(q if q_host is None else q_host, last_ids, last_valid, out=out_host,
-                          refresh_last=refresh_last)
-                return
             if q_host is not None:
                 q.copy_(q_host, non_blocking=True)
+            if zero_copy:
+                self.step(q, last_ids, last_valid, out=out_host, refresh_last=refresh_last)
+                return
             self.step(q, last_ids, last_valid, refresh_last=refresh_last)
             if out_host is not None:
                 out_host.copy_(self.out, non_blocking=True)
