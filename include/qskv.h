@@ -257,9 +257,18 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
  *   lse[b][h] = log sum_t exp(l_t).
  * selected == NULL means every page j < n_b (exact dense paged decode);
  * n_selected and top_k are then ignored.  sm_scale == 0 means 1/sqrt(d).
- * A row split over several decode warps is combined either by the last of
- * those warps (when its pieces fit one warp's single round of loads; a
- * per-row counter in the workspace picks that warp) or by a second kernel.
+ * Work split: when the (sequence, KV head) rows fit one wave of decode CTAs
+ * (at most two per SM, at most 1024 units per row), each row goes to k CTAs
+ * (k = 1 with at least one row per SM, else up to 8) whose warps' partial
+ * results are combined in the CTA and, with k > 1, across the k CTAs by the
+ * CTA drawing the row's last ticket (a per-row counter in the workspace);
+ * otherwise the units are split evenly over the warps of a persistent grid
+ * and a split row is combined by its last warp (when its pieces fit one
+ * warp's single round of loads) or by a second kernel.  The per-row
+ * counters are zero between calls (a zeroed workspace starts them so).
+ * q, page_table and seq_lens may be read before the previous kernel in the
+ * stream has completed when that kernel is one of this library's (which
+ * never writes them); a kernel of the caller's is always waited for.
  * A sequence with no token gives out = 0 and lse = -inf.  lse may be NULL.
  * Device errors: a bad page id or selected index skips that page and flags
  * QSKV_ERR_DEVICE_INDEX.
