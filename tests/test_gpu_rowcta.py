@@ -96,3 +96,40 @@ def test_row_per_cta_matches_the_oracle(oracle_lib, kind):
             first = (dec.out.clone(), dec.lse.clone())
         else:
             assert torch.equal(dec.out, first[0]) and torch.equal(dec.lse, first[1]), f"call {it} differs"
+
+
+def _edge_spec(kind):
+    """Rows of no, one, two and many pages in the one-row-per-CTA split:
+    with k = 1 (one row per SM or more) and with k = 8 (CTAs left without
+    units give empty pieces)."""
+    sms = _sms()
+    if kind == "edge_k1":
+        batch = -(-sms // 8) + 1
+        lens = [0, 1, 15, 16, 17, 33] + [3000 + 97 * i for i in range(batch - 6)]
+        return W.spec_for("llama3_8b", batch=batch, seq_lens=tuple(lens), seq_len_range=None, max_pages=None,
+                          top_k=64, kind="iid")
+    return W.spec_for("long_context", batch=3, seq_lens=(0, 40, 5000), seq_len_range=None, max_pages=None,
+                      top_k=64, kind="iid")
+
+
+@pytest.mark.parametrize("kind", ["edge_k1", "edge_k8"])
+def test_row_per_cta_short_and_empty_rows(oracle_lib, kind):
+    spec = _edge_spec(kind)
+    inp = W.make_inputs(spec)
+    rows = spec.batch * spec.num_kv_heads
+    k = row_blocks(rows, spec.top_k, _sms())
+    assert k == (1 if kind == "edge_k1" else 8), f"unexpected split (k = {k})"
+    dec = qskv.from_inputs(inp)
+    ids, vt = oracle_lib.all_pages(inp)
+    dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    dec.select()
+    dec.out.fill_(float("nan"))
+    dec.lse.fill_(float("nan"))
+    dec.decode()
+    dec.check()
+    torch.cuda.synchronize()
+    # the sequence with no token: output 0, lse -inf, nothing selected
+    assert (dec.n_selected[0] == 0).all()
+    assert (dec.out[0] == 0).all() and torch.isneginf(dec.lse[0]).all()
+    check = [r for r in range(rows) if r >= spec.num_kv_heads]
+    PR.check_rows(inp, dec, check, oracle_lib, oracle_meta=oracle_lib.meta(inp["k_pool"], ids, vt))
