@@ -708,8 +708,22 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
         k = 1 if rows >= sms else min(ctas // rows, 8, spr // 4)
         k = k if k == 1 or (k >= 2 and rows * k >= sms) else 0
     row_per_cta = k > 0
-    fold = row_per_cta or (spec.kv_dtype == torch.bfloat16 and prefix == 0
-                           and pieces * max(1, spec.group * spec.head_dim // 128) <= 16)
+    per_lane = max(1, spec.group * spec.head_dim // 128)
+    fold = row_per_cta or (spec.kv_dtype == torch.bfloat16 and prefix == 0 and pieces * per_lane <= 16)
+    if prefix and spec.kv_dtype == torch.bfloat16:
+        # the cascade: its decode grid is sized to the SMs the prefix grid
+        # leaves, and a row also holds the prefix kernel's E pieces
+        # (prefix_splits / prefix_ctas in prefix_attend.cu)
+        tiles = -(-spec.batch * spec.group // 128) * spec.num_kv_heads
+        nblk = -(-prefix * spec.page_size // 128)
+        e = max(1, min(sms // tiles, nblk, 64)) if nblk else 0
+        items = tiles * e
+        share = max(1, int(sms * 0.43))
+        rounds = -(-items // share)
+        pctas = -(-items // rounds) if items else 0
+        warps = 2 * max(1, sms - pctas) * 6
+        upw_c = max(1, -(-rows * spr // warps))
+        fold = spr > 0 and (-(-spr // upw_c) + 1 + e) * per_lane <= 16
     # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV
     fused_refresh = spec.kv_dtype == torch.bfloat16 and scorer == "bound" and not approx
     n = ((2 if fused_refresh else 3) if spec.top_k is not None else 0) + 1 + (0 if fold else 1)

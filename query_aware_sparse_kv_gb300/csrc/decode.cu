@@ -132,8 +132,11 @@ __device__ void fold_row_warp(const DecodeArgs &a, int row, int64_t w0, int64_t 
     constexpr int BATCH = 16 / CPL;
     const int lane = threadIdx.x & 31;
     if (COLS < 32 && lane >= COLS) return;
-    const int n = int(w1 - w0 + 1);
-    const int64_t slot0 = row + w0;
+    // pieces: the decode warps' (slots row + w0 ..) then another kernel's
+    // extra pieces (slots extra_slot0 + row * extra_pieces ..)
+    const int nd = int(w1 - w0 + 1);
+    const int n = nd + a.extra_pieces;
+    const int64_t slot0 = row + w0, eslot0 = a.extra_slot0 + int64_t(row) * a.extra_pieces;
     const float4 *o_all = reinterpret_cast<const float4 *>(a.part_o);
     float mx[CPL], den[CPL];
     float4 acc[CPL];
@@ -152,7 +155,7 @@ __device__ void fold_row_warp(const DecodeArgs &a, int row, int64_t w0, int64_t 
             for (int j = 0; j < CPL; j++) {
                 const int c = lane + 32 * j;
                 const bool ok = p0 + k < n;
-                const int64_t s = slot0 + p0 + k;
+                const int64_t s = p0 + k < nd ? slot0 + p0 + k : eslot0 + (p0 + k - nd);
                 l[k][j] = ok ? __ldcg(a.part_lse + s * G + c / V4) : -INFINITY;
                 v[k][j] = ok ? __ldcg(o_all + s * COLS + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -204,18 +207,18 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
     const int lane = threadIdx.x & 31;
     __threadfence();  // this lane's piece stores, before the tickets
     __syncwarp();
-    for (int k = 0; k < 2; k++) {
-        const int row = k == 0 ? row_first : row_last;
-        if (k == 1 && row_last == row_first) break;
+    for (int row = row_first; row <= row_last; row++) {
         int64_t w0, w1;
         row_warps(a, row, w0, w1);
         if (row_is_final(a, w0, w1)) continue;  // this warp wrote the row's output itself
-        uint32_t last = 0;
-        if (lane == 0) {
-            last = atomicAdd(a.tickets + row, 1u) == uint32_t(w1 - w0) ? 1u : 0u;
-            if (last) __threadfence();  // the other warps' pieces, before they are read
+        if (w0 < w1) {  // shared with other decode warps: the last ticket folds
+            uint32_t last = 0;
+            if (lane == 0) {
+                last = atomicAdd(a.tickets + row, 1u) == uint32_t(w1 - w0) ? 1u : 0u;
+                if (last) __threadfence();  // the other warps' pieces, before they are read
+            }
+            if (!__shfl_sync(0xffffffffu, last, 0)) continue;
         }
-        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
         switch (a.group) {
             case 1: fold_row_warp<D, 1>(a, row, w0, w1); break;
             case 2: fold_row_warp<D, 2>(a, row, w0, w1); break;
@@ -223,7 +226,7 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
             default: fold_row_warp<D, 8>(a, row, w0, w1); break;
         }
         __syncwarp();
-        if (lane == 0) a.tickets[row] = 0u;
+        if (lane == 0 && w0 < w1) a.tickets[row] = 0u;
     }
 }
 
@@ -622,8 +625,8 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                 break;
             }
             // keep the row counters consistent (the outputs are flagged as invalid)
-            if (a.fold) fold_shared_rows<D>(a, row_begin, row_last);
             if (a.wait_at_exit) pdl_wait();
+            if (a.fold) fold_shared_rows<D>(a, row_begin, row_last);
             return;
         }
         const int row = __shfl_sync(0xffffffffu, st_row, cs);
@@ -819,8 +822,8 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     if (cur_row >= 0) finish_row(cur_row);
     for (int r = empty_from; r <= row_last; r++)
         if (r != cur_row) write_empty_piece<D>(a, r, gw);
+    if (a.wait_at_exit) pdl_wait();  // a cascade: the prefix kernel's pieces are complete
     if (a.fold) fold_shared_rows<D>(a, row_begin, row_last);
-    if (a.wait_at_exit) pdl_wait();
 }
 
 // --------------------------------------------------- fp32 KV, CUDA cores --
@@ -1052,10 +1055,18 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
         if (kv_dtype != kDtypeBf16) return cudaErrorInvalidValue;
         cudaError_t e = launch_prefix(*prefix, tmap_k, tmap_v, q_dtype, head_dim, stream);
         if (e != cudaSuccess) return e;
+        // a row's decode pieces and the prefix kernel's are folded by the
+        // decode warp that finishes the row last (after its wait for the
+        // prefix grid) when one warp can load them in one round; otherwise
+        // by the merge kernel
+        const int64_t upw_c = a.units_per_warp > 0 ? a.units_per_warp : 1;
+        const int64_t pieces_c = (a.slots_per_row + upw_c - 1) / upw_c + 1 + a.extra_pieces;
+        const int64_t per_lane_c = a.group * head_dim / 128 > 1 ? a.group * head_dim / 128 : 1;
+        const bool fold_c = a.total_units > 0 && a.tickets != nullptr && pieces_c * per_lane_c <= kFoldMaxLoads;
         if (a.total_units > 0) {
             DecodeArgs d = da;
             d.wait_at_exit = 1;
-            d.fold = 0;  // the prefix kernel's pieces are merged by the merge kernel
+            d.fold = fold_c ? 1 : 0;
             if (head_dim == 128)
                 e = qf ? launch_bf16<128, true>(d, tmap_k, tmap_v, grid, stream)
                        : launch_bf16<128, false>(d, tmap_k, tmap_v, grid, stream);
@@ -1064,7 +1075,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap *tmap_k, const 
                        : launch_bf16<64, false>(d, tmap_k, tmap_v, grid, stream);
             if (e != cudaSuccess) return e;
         }
-        return launch_merge(a, head_dim, stream);
+        return fold_c ? cudaSuccess : launch_merge(a, head_dim, stream);
     }
     if (a.total_units == 0) return cudaSuccess;
     if (kv_dtype == kDtypeBf16) {
