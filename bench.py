@@ -521,6 +521,22 @@ class Bench:
         self.use(v)
         self.dec.decode(q=self.qv[v])
 
+    @property
+    def one_call(self) -> bool:
+        """Whether a step is PagedDecoder.step's single call (qskv_select_decode:
+        scoring with the last-page refresh, then the decode, which ranks its own
+        rows when they go one row per k CTAs)."""
+        return (self.spec.top_k is not None and self.dec.can_refresh_in_select
+                and not self.args.separate_calls)
+
+    def step_part(self, v: int):
+        if self.one_call:
+            self.use(v)
+            self.dec.step(q=self.qv[v], refresh_last=True)
+        else:
+            self.select_part(v)
+            self.decode_part(v)
+
     @staticmethod
     def capture(fn):
         side = torch.cuda.Stream()
@@ -552,12 +568,10 @@ class Bench:
 
     def build_graphs(self, warmup: int):
         for i in range(warmup):
-            self.select_part(i % N_Q_VARIANTS)
-            self.decode_part(i % N_Q_VARIANTS)
+            self.step_part(i % N_Q_VARIANTS)
         self.dec.check()
         torch.cuda.synchronize()
-        self.step_graphs = [self.capture(lambda v=v: (self.select_part(v), self.decode_part(v)))
-                            for v in range(N_Q_VARIANTS)]
+        self.step_graphs = [self.capture(lambda v=v: self.step_part(v)) for v in range(N_Q_VARIANTS)]
         self.sel_graphs = [self.capture(lambda v=v: self.select_part(v)) for v in range(N_Q_VARIANTS)]
         self.dec_graphs = [self.capture(lambda v=v: self.decode_part(v)) for v in range(N_Q_VARIANTS)]
         for i in range(warmup):
@@ -647,8 +661,7 @@ class Bench:
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(n):
-            self.select_part(i % N_Q_VARIANTS)
-            self.decode_part(i % N_Q_VARIANTS)
+            self.step_part(i % N_Q_VARIANTS)
         e1.record(stream)
         torch.cuda.synchronize()
         self.dec.check()
@@ -668,7 +681,7 @@ class Bench:
         graphs = []
         for v in range(N_Q_VARIANTS):
             self.use(v)
-            fused = spec.top_k is not None and dec.can_refresh_in_select
+            fused = spec.top_k is not None and dec.can_refresh_in_select and not self.args.separate_calls
             refresh = self.last[self.table_for(v)] if spec.top_k is not None and not fused else (None, None)
             graphs.append(dec.capture_step(q_dev, *refresh, q_host=q_host[v], out_host=out_host,
                                            zero_copy=zero_copy, refresh_last=fused))
@@ -687,10 +700,12 @@ class Bench:
         return world * steps / s
 
 
-def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bound", approx: bool = False) -> int:
+def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bound", approx: bool = False,
+                     one_call: bool = True) -> int:
     """The library's launches in one step: metadata refresh (inside the
     scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
-    (sparse only), decode, and the merge kernel unless the decode folds the
+    (sparse only; inside the decode launch when the step is one call and the
+    rows go one row per k CTAs), decode, and the merge kernel unless the decode folds the
     rows' pieces itself: bf16 KV without a shared prefix, and either the rows
     fit one wave of decode CTAs (one row per k CTAs: k = 1 for one or two rows
     per SM, else min(2 SMs / rows, 8, units / 4) when that gives every SM a
@@ -726,7 +741,9 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
         fold = spr > 0 and (-(-spr // upw_c) + 1 + e) * per_lane <= 16
     # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV
     fused_refresh = spec.kv_dtype == torch.bfloat16 and scorer == "bound" and not approx
-    n = ((2 if fused_refresh else 3) if spec.top_k is not None else 0) + 1 + (0 if fold else 1)
+    ranked_in_decode = fused_refresh and one_call and row_per_cta
+    n = ((2 if fused_refresh else 3) - (1 if ranked_in_decode else 0) if spec.top_k is not None else 0) + 1 + \
+        (0 if fold else 1)
     return n + (1 if prefix else 0)
 
 
@@ -823,7 +840,8 @@ def run_gpu(args):
             ent["config"] = workload_config(ws, args.scorer, args.approx_eps, bn.inputs, bn.replicas)
             ent["steps"] = args.sub_steps
             ent["recall"] = rec
-            ent["kernels_per_step"] = kernels_per_step(ws, bn.inputs, bn.prefix, args.scorer, args.approx_eps is not None)
+            ent["kernels_per_step"] = kernels_per_step(ws, bn.inputs, bn.prefix, args.scorer, args.approx_eps is not None,
+                                               not args.separate_calls)
             if sampler:
                 ent["clocks"] = sampler.summary(t0, t1)
             if not args.no_cpu_baseline:
@@ -861,8 +879,10 @@ def run_gpu(args):
                      "traffic": ncu_traffic(args.workload), "decode_src_sha256_16": source_hash(DECODE_SOURCES)},
         "cpu_baseline": cpu,
         "recall": recall,
-        "step_launch": ("CUDA graph replay, one graph per query variant (last-page metadata refresh inside the "
-                        "scoring launch + ranking + decode)"
+        "step_launch": ("CUDA graph replay, one graph per query variant: " +
+                        ("qskv_select_decode (scoring launch with the last-page metadata refresh inside, then the "
+                         "decode launch, which ranks its own rows when they go one row per k CTAs)" if main.one_call
+                         else "scoring (last-page metadata refresh inside where it can be) + ranking + decode")
                         if spec.top_k is not None else
                         "CUDA graph replay, one graph per query variant (dense decode: no metadata refresh or selection)"),
         "eager_ms_per_step": eager_ms,
@@ -872,10 +892,11 @@ def run_gpu(args):
                         "waits for every step (PagedDecoder.wait)",
                 "copy_nodes_value": e2e_copy_nodes,
                 "h2d_bytes_per_step": getattr(main, "e2e_h2d", 0), "d2h_bytes_per_step": getattr(main, "e2e_d2h", 0)},
-        # kernels per step: metadata refresh (fused into scoring where it can be), scoring, ranking,
-        # decode, merge (dense: decode and merge only; cascade: + the shared-prefix kernel; no merge
-        # when the decode folds its split rows)
-        "gpu_launches": kernels_per_step(spec, main.inputs, prefix, args.scorer, args.approx_eps is not None) * args.steps,
+        # kernels per step: metadata refresh (fused into scoring where it can be), scoring, ranking
+        # (inside the decode for one-call steps of one row per k CTAs), decode, merge (dense: decode
+        # and merge only; cascade: + the shared-prefix kernel; no merge when the decode folds its rows)
+        "gpu_launches": kernels_per_step(spec, main.inputs, prefix, args.scorer, args.approx_eps is not None,
+                                         not args.separate_calls) * args.steps,
         "clocks": clocks,
         "per_workload": per_workload or None,
     }
@@ -912,6 +933,8 @@ def main(argv=None):
                     help="time only --workload (profiling runs); by default the other workloads follow")
     ap.add_argument("--sub-steps", type=int, default=1000, help="timed steps of each other workload")
     ap.add_argument("--no-recall", action="store_true", help="skip the recall figures of the selection")
+    ap.add_argument("--separate-calls", action="store_true",
+                    help="a step as the separate selection and decode calls instead of qskv_select_decode")
     ap.add_argument("--no-cascade", action="store_true",
                     help="shared-prefix workload: plain paged dense decode instead of the cascade")
     args = ap.parse_args(argv)

@@ -9,7 +9,8 @@
  *                            split over warps and merged by log-sum-exp
  *
  * (qskv_page_select_refresh does the first two in one launch: the last
- * pages' metadata refresh inside the scoring grid),
+ * pages' metadata refresh inside the scoring grid; qskv_select_decode does
+ * the whole step in one call, two launches),
  *
  * with an alternative block score (the mean key of each page, "Block Top-K"):
  *
@@ -278,6 +279,29 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
                                      const qskv_shape *shape, const int32_t *selected, const int32_t *n_selected,
                                      int32_t top_k, float sm_scale, float *out, float *lse, void *workspace,
                                      size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step in one call (TinyServe query-aware page selection, s2.3:
+ * score every page from its metadata, keep the top-K, load only those pages
+ * and attend; s3.2 fuses those stages into one kernel; s5.3: the metadata of
+ * the page the new token went into is refreshed every step).  The result is
+ * exactly qskv_page_select_refresh(q, k_pool, meta, ..., top_k, selected,
+ * n_selected, scores) followed by qskv_sparse_paged_decode(q, k_pool,
+ * v_pool, ..., selected, n_selected, top_k, sm_scale, out, lse): the same
+ * metadata update, the same selection (written to selected / n_selected, and
+ * the scores to `scores` when it is not NULL), the same outputs.  Two
+ * launches: the scoring grid (with the refresh), then the decode, whose CTAs
+ * rank their own rows first when the rows go one row per k CTAs (see
+ * qskv_sparse_paged_decode); otherwise the ranking kernel runs in between.
+ * bf16 KV only (QSKV_ERR_UNSUPPORTED otherwise); q fp32 or bf16; exact top-K
+ * with the bound score.  Workspace: qskv_workspace_size(shape).  Same
+ * argument checks and device errors as the two calls.
+ */
+qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool, void *meta,
+                               qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                               const qskv_shape *shape, int32_t top_k, float sm_scale, int32_t *selected,
+                               int32_t *n_selected, float *scores, float *out, float *lse, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /*
  * qskv_sparse_paged_decode without a workspace, for callers that cannot

@@ -11,6 +11,9 @@ in include/qskv.h); this package is its binding:
   page_select_centroid   with the same top-K
   page_select_approx   either score with a lossy top-K (early exit + sampling)
   sparse_paged_decode  split-K attention over the selected pages, LSE merge
+  select_decode        one step in one call: last-page refresh, scoring,
+                       top-K and the sparse decode (the decode ranks its
+                       own rows when they go one row per k CTAs)
   cascade_paged_decode dense decode of a batch sharing a page prefix: the
                        prefix once per KV head on the tensor cores, the rest
                        paged, LSE merge
@@ -21,12 +24,13 @@ built library every call raises.
 """
 from .binding import (QSKV_BF16, QSKV_F32, QskvError, QskvLibraryMissing, Shape, cascade_paged_decode,
                       cascade_workspace_size, get_error, kv_centroid_build, kv_meta_build, last_error_message, load,
-                      make_shape, page_select, page_select_approx, page_select_refresh, page_select_centroid, sparse_paged_decode,
-                      sparse_paged_decode_noalloc, workspace_size)
+                      make_shape, page_select, page_select_approx, page_select_refresh, page_select_centroid,
+                      select_decode, sparse_paged_decode, sparse_paged_decode_noalloc, workspace_size)
 from .engine import PagedDecoder, from_inputs
 
 __all__ = ["QSKV_BF16", "QSKV_F32", "QskvError", "QskvLibraryMissing", "Shape", "cascade_paged_decode",
            "cascade_workspace_size", "get_error", "kv_centroid_build", "kv_meta_build", "page_select_approx", "page_select_centroid",
-           "last_error_message", "load", "make_shape", "page_select", "page_select_refresh", "sparse_paged_decode",
+           "last_error_message", "load", "make_shape", "page_select", "page_select_refresh", "select_decode",
+           "sparse_paged_decode",
            "sparse_paged_decode_noalloc", "workspace_size",
            "PagedDecoder", "from_inputs"]

@@ -23,10 +23,10 @@ STATUS = {0: "QSKV_OK", 1: "QSKV_ERR_INVALID_ARG", 2: "QSKV_ERR_UNSUPPORTED", 3:
 
 # Every function the header declares, in declaration order.
 EXPORTS = ("qskv_workspace_size", "qskv_kv_meta_build", "qskv_page_select", "qskv_page_select_refresh",
-           "qskv_kv_centroid_build",
-           "qskv_page_select_centroid", "qskv_page_select_approx", "qskv_sparse_paged_decode",
-           "qskv_sparse_paged_decode_noalloc", "qskv_cascade_workspace_size", "qskv_cascade_paged_decode",
-           "qskv_get_error", "qskv_status_string", "qskv_last_error_message")
+           "qskv_kv_centroid_build", "qskv_page_select_centroid", "qskv_page_select_approx",
+           "qskv_sparse_paged_decode", "qskv_select_decode", "qskv_sparse_paged_decode_noalloc",
+           "qskv_cascade_workspace_size", "qskv_cascade_paged_decode", "qskv_get_error", "qskv_status_string",
+           "qskv_last_error_message")
 
 
 class QskvLibraryMissing(RuntimeError):
@@ -82,6 +82,9 @@ def load(path: str = LIB_PATH):
     lib.qskv_sparse_paged_decode.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p, i32p, i32,
                                              ctypes.c_float, f32p, f32p, vp, sz, vp]
+    lib.qskv_select_decode.restype = ctypes.c_int
+    lib.qskv_select_decode.argtypes = [vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, i32p, i32p, sp, i32, ctypes.c_float,
+                                       i32p, i32p, f32p, f32p, f32p, vp, sz, vp]
     lib.qskv_sparse_paged_decode_noalloc.restype = ctypes.c_int
     lib.qskv_sparse_paged_decode_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, i32p, i32p, sp, i32p,
                                                      i32p, i32, ctypes.c_float, f32p, f32p, vp]
@@ -163,6 +166,21 @@ def page_select_refresh(q: torch.Tensor, k_pool: torch.Tensor, meta: torch.Tenso
                                            _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(top_k),
                                            _ptr(selected), _ptr(n_selected), _ptr(scores), _ptr(workspace),
                                            workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def select_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, meta: torch.Tensor,
+                  page_table: torch.Tensor, seq_lens: torch.Tensor, top_k: int, selected: torch.Tensor,
+                  n_selected: torch.Tensor, out: torch.Tensor, shape: Shape, workspace: torch.Tensor,
+                  lse: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
+                  stream=None):
+    """One decode step: last-page metadata refresh, bound scores, exact top-K
+    and the sparse decode (two launches; the decode ranks its own rows when
+    they go one row per k CTAs)."""
+    _check(load().qskv_select_decode(_ptr(q), _dtype(q), _ptr(k_pool), _ptr(v_pool), _ptr(meta), _dtype(k_pool),
+                                     _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(top_k),
+                                     float(sm_scale), _ptr(selected), _ptr(n_selected), _ptr(scores), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def kv_centroid_build(k_pool: torch.Tensor, page_ids: torch.Tensor, valid_tokens: torch.Tensor,

@@ -43,6 +43,7 @@
 
 #include "qskv_device.cuh"
 #include "qskv_internal.h"
+#include "qskv_select.cuh"
 
 namespace qskv {
 namespace {
@@ -82,6 +83,23 @@ __device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot,
     } else if (j >= n_b) {
         return -1;
     }
+    const int p = pt_row ? pt_row[j] : __ldg(a.page_table + int64_t(b) * a.max_pages + j);
+    if (p < 0 || p >= a.num_pool_pages) {
+        raise_error(a.flags, kErrPageId);
+        return -1;
+    }
+    return (p << 6) | min(a.page_size, seq - j * a.page_size);
+}
+
+// Code of logical page j of row `row` (a selected index the caller did not
+// pass: the fused rank + decode), with unit_code's checks.
+__device__ __forceinline__ int page_code(const DecodeArgs &a, int row, int j, const int32_t *pt_row) {
+    const int b = row / a.num_kv_heads;
+    int seq = __ldg(a.seq_lens + b);
+    const int cap = a.max_pages * a.page_size;
+    seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
+    const int n_b = (seq + a.page_size - 1) / a.page_size;
+    if (j < 0 || j >= n_b) return -1;
     const int p = pt_row ? pt_row[j] : __ldg(a.page_table + int64_t(b) * a.max_pages + j);
     if (p < 0 || p >= a.num_pool_pages) {
         raise_error(a.flags, kErrPageId);
@@ -246,7 +264,7 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // with k > 1 into one piece per block in the workspace, and the block that
 // draws the row's last ticket (a per-row counter; no block waits for
 // another) folds the k pieces with all its threads and resets the counter.
-template <int D, bool QF32, int WPC, int HALVES, bool HINT, bool ROWCTA>
+template <int D, bool QF32, int WPC, int HALVES, bool HINT, bool ROWCTA, bool RANK = false>
 __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        DecodeArgs a) {
@@ -310,8 +328,34 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     if (!a.wait_at_exit) pdl_wait();
     if constexpr (ROWCTA) {
         __syncthreads();
-        for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
-            s_code[i] = unit_code(a, rc_row, i, a.pt_in_smem ? s_pt : nullptr);
+        if constexpr (RANK) {
+            // Fused rank + decode: the CTA ranks its row's scores first (the
+            // ranking kernel's routine; keys in the ring's memory, the list in
+            // s_code), then turns each selected page into its code in place.
+            __shared__ uint32_t r_hist[256], r_mm[2 * WPC];
+            __shared__ int r_tmp[2 * WPC], r_pick[3];
+            const SelectSmem sm{reinterpret_cast<uint32_t *>(ring0), r_hist, r_mm, r_tmp, r_pick};
+            SelectArgs sa{};
+            sa.selected = a.selected_out;
+            sa.n_selected = a.n_selected_out;
+            sa.top_k = a.top_k;
+            sa.need_max = 0;
+            sa.seed = 0;
+            const int b = rc_row / a.num_kv_heads;
+            int seq = __ldg(a.seq_lens + b);
+            const int cap = a.max_pages * a.page_size;
+            seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
+            const int n_b = (seq + a.page_size - 1) / a.page_size;
+            const int nsel = select_row<WPC * 32>(sa, rc_row, n_b, a.scores + int64_t(rc_row) * a.max_pages, sm,
+                                                  s_code, rc_blk == 0);
+            fence_proxy_async_smem();  // the keys' stores, before TMA refills of the same memory
+            __syncthreads();
+            for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
+                s_code[i] = i < nsel ? page_code(a, rc_row, s_code[i], a.pt_in_smem ? s_pt : nullptr) : -1;
+        } else {
+            for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
+                s_code[i] = unit_code(a, rc_row, i, a.pt_in_smem ? s_pt : nullptr);
+        }
         __syncthreads();
     }
     // K/V streams larger than L2 are read evict-first; smaller ones with no
@@ -924,7 +968,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
     if (cur_row >= 0) finish_row(cur_row);
 }
 
-template <int D, bool QF32, bool HINT, bool ROWCTA>
+template <int D, bool QF32, bool HINT, bool ROWCTA, bool RANK = false>
 cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                              const DecodeGrid &grid, cudaStream_t stream) {
     constexpr int WPC = D == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64;
@@ -933,7 +977,7 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     // ROWCTA: the row's unit codes after the rings, then its page-table row if staged
     const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? rowcta_extra_smem(a, D * (QF32 ? 4 : 2)) : 0);
     const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads * a.row_blocks) : unsigned(grid.ctas);
-    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA>;
+    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA, RANK>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
     static std::mutex mu;                // calls may come from several host threads
     int dev = 0;
@@ -952,6 +996,9 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
 template <int D, bool QF32>
 cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
                         cudaStream_t stream, bool rowcta = false) {
+    if (rowcta && a.scores)  // fused rank + decode
+        return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true, true>(a, tk, tv, grid, stream)
+                                : launch_bf16_hint<D, QF32, false, true, true>(a, tk, tv, grid, stream);
     if (rowcta)
         return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true>(a, tk, tv, grid, stream)
                                 : launch_bf16_hint<D, QF32, false, true>(a, tk, tv, grid, stream);

@@ -465,6 +465,113 @@ qskv_status qskv_page_select_approx(qskv_scorer scorer, const void *q, qskv_dtyp
     return launched(e, "page_select_approx launch");
 }
 
+qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool, void *meta,
+                               qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
+                               const qskv_shape *shape, int32_t top_k, float sm_scale, int32_t *selected,
+                               int32_t *n_selected, float *scores, float *out, float *lse, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    QSKV_TRY(check_shape(shape));
+    QSKV_TRY(check_dtype(q_dtype, "q"));
+    QSKV_TRY(check_dtype(kv_dtype, "kv"));
+    if (kv_dtype != QSKV_BF16)
+        return fail(QSKV_ERR_UNSUPPORTED, "qskv_select_decode needs a bf16 KV cache (use the separate calls)");
+    if (top_k < 1) return fail(QSKV_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", top_k);
+    if (!q || !k_pool || !v_pool || !meta || !page_table || !seq_lens || !selected || !n_selected || !out)
+        return fail(QSKV_ERR_INVALID_ARG,
+                    "q, k_pool, v_pool, meta, page_table, seq_lens, selected, n_selected and out must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(meta, 16) || !aligned(out, 16))
+        return fail(QSKV_ERR_INVALID_ARG, "q, k_pool, v_pool, meta and out must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(selected, 4) || !aligned(n_selected, 4) ||
+        !aligned(scores, 4) || !aligned(lse, 4))
+        return fail(QSKV_ERR_INVALID_ARG, "index, score and lse arrays must be 4-byte aligned");
+    if (!(sm_scale >= 0.f) || isinf(sm_scale)) return fail(QSKV_ERR_INVALID_ARG, "sm_scale must be finite and >= 0");
+    const int sms = current_sm_count(nullptr);
+    if (sms <= 0) return fail(QSKV_ERR_CUDA, "cannot query the current CUDA device");
+    const int64_t rows = int64_t(shape->batch) * shape->num_kv_heads;
+    const int G = shape->num_q_heads / shape->num_kv_heads;
+    const WorkspaceLayout L = workspace_layout(rows, G, shape->head_dim, shape->max_pages, sms);
+    QSKV_TRY(check_workspace(workspace, workspace_bytes, L.total));
+    const DecodeGrid grid = decode_grid(sms, shape->head_dim);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *sc = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
+    uint32_t *tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
+    // the decode ranks its own rows when they go one row per k CTAs
+    const bool fused = row_blocks_for(rows, top_k, grid.ctas, true, true) > 0;
+
+    SelectArgs sa;
+    sa.k_pool = k_pool;
+    sa.meta_w = meta;
+    sa.q = q;
+    sa.meta = meta;
+    sa.page_table = page_table;
+    sa.seq_lens = seq_lens;
+    sa.selected = selected;
+    sa.n_selected = n_selected;
+    sa.scores = sc;
+    sa.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    sa.batch = shape->batch;
+    sa.num_q_heads = shape->num_q_heads;
+    sa.num_kv_heads = shape->num_kv_heads;
+    sa.group = G;
+    sa.page_size = shape->page_size;
+    sa.max_pages = shape->max_pages;
+    sa.num_pool_pages = shape->num_pool_pages;
+    sa.top_k = top_k;
+    sa.need_max = 0;
+    sa.seed = 0;
+    sa.meta_evict_first = 0;
+    sa.head_quads = 0;
+    QSKV_TRY(launched(launch_page_select(sa, q_dtype, QSKV_BF16, shape->head_dim, st, scores != nullptr, 1,
+                                         fused ? 0 : 1),
+                      "select_decode scoring launch"));
+
+    DecodeArgs a;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = reinterpret_cast<float *>(ws + L.part_o);
+    a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+    a.batch = shape->batch;
+    a.num_q_heads = shape->num_q_heads;
+    a.num_kv_heads = shape->num_kv_heads;
+    a.group = G;
+    a.page_size = shape->page_size;
+    a.max_pages = shape->max_pages;
+    a.num_pool_pages = shape->num_pool_pages;
+    a.top_k = top_k;
+    a.slots_per_row = top_k;
+    a.page_begin = 0;
+    a.extra_pieces = 0;
+    a.extra_slot0 = 0;
+    a.wait_at_exit = 0;
+    a.kv_evict_first = 0;
+    a.stages = decode_stages(shape->head_dim);
+    a.tickets = tickets;
+    a.fold = 0;
+    a.total_units = rows * a.slots_per_row;
+    a.units_per_warp = (a.total_units + grid.total_warps - 1) / grid.total_warps;
+    const float scale = sm_scale > 0.f ? sm_scale : 1.f / sqrtf(float(shape->head_dim));
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (fused) {
+        a.scores = sc;
+        a.selected_out = selected;
+        a.n_selected_out = n_selected;
+    }
+    CUtensorMap tk, tv;
+    QSKV_TRY(make_pool_map(&tk, k_pool, shape));
+    QSKV_TRY(make_pool_map(&tv, v_pool, shape));
+    return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, st),
+                    "select_decode decode launch");
+}
+
 qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const void *k_pool, const void *v_pool,
                                      qskv_dtype kv_dtype, const int32_t *page_table, const int32_t *seq_lens,
                                      const qskv_shape *shape, const int32_t *selected, const int32_t *n_selected,

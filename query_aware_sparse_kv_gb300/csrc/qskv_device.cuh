@@ -501,6 +501,12 @@ struct DecodeArgs {
     int32_t row_blocks = 1; // one-row-per-CTA decode: CTAs per row (1: the CTA finishes the row)
     int32_t pt_in_smem = 0; // one-row-per-CTA decode: the row's page-table entries are staged in
                             // shared memory before the wait for the previous kernel
+    // Fused rank + decode (one row per k CTAs): each CTA first ranks its row's
+    // `scores` (top_k, exact) itself; block 0 of the row writes the list and
+    // count to selected_out / n_selected_out.
+    const float *scores = nullptr;
+    int32_t *selected_out = nullptr;
+    int32_t *n_selected_out = nullptr;
 };
 
 // Shared-prefix cascade: the attention of all B x G query rows of one KV head

@@ -50,7 +50,7 @@ cudaError_t launch_page_select_centroid(const SelectArgs &a, int q_dtype, int he
 // score_all: compute scores even for rows where every page is kept.
 // refresh: recompute each row's last-page metadata from a.k_pool first (bf16 only).
 cudaError_t launch_page_select(const SelectArgs &a, int q_dtype, int meta_dtype, int head_dim, cudaStream_t stream,
-                               int score_all, int refresh = 0);
+                               int score_all, int refresh = 0, int rank = 1);
 // tmap_k / tmap_v are used by the bf16 tensor-core kernels only.  With
 // `prefix` (a cascade decode, bf16 KV) the shared-prefix kernel runs between
 // the decode and the merge.

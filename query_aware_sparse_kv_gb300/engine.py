@@ -125,7 +125,15 @@ class PagedDecoder:
         """Metadata refresh of the pages being appended to, selection, decode
         (into ``out`` if given, else ``self.out``).  The refresh is either
         the listed pages (last_ids, last_valid) or, with refresh_last, every
-        sequence's last page inside the selection's launch."""
+        sequence's last page inside the selection's launch; then, where the
+        selection can take the refresh (bound scorer, exact top-K, bf16 KV),
+        the whole step is one call (qskv_select_decode)."""
+        if refresh_last and last_ids is None and self.top_k is not None and self.can_refresh_in_select:
+            B.select_decode(self.q if q is None else q, self.k_pool, self.v_pool, self.meta, self.page_table,
+                            self.seq_lens, self.top_k, self.selected, self.n_selected,
+                            self.out if out is None else out, self.shape, self.workspace, lse=self.lse,
+                            sm_scale=self.sm_scale, stream=stream)
+            return
         if last_ids is not None:
             self.build_meta(last_ids, last_valid, stream)
         if self.top_k is not None:
