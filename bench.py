@@ -705,7 +705,9 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
     """The library's launches in one step: metadata refresh (inside the
     scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
     (sparse only; inside the decode launch when the step is one call and the
-    rows go one row per k CTAs), decode, and the merge kernel unless the decode folds the
+    rows go one row per k CTAs, and the scoring with the refresh too when
+    k >= 2 and a CTA's share of the pages fits one staging round), decode,
+    and the merge kernel unless the decode folds the
     rows' pieces itself: bf16 KV without a shared prefix, and either the rows
     fit one wave of decode CTAs (one row per k CTAs: k = 1 for one or two rows
     per SM, else min(2 SMs / rows, 8, units / 4) when that gives every SM a
@@ -742,8 +744,13 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
     # the refresh runs inside the scoring launch for the exact bound top-K on bf16 KV
     fused_refresh = spec.kv_dtype == torch.bfloat16 and scorer == "bound" and not approx
     ranked_in_decode = fused_refresh and one_call and row_per_cta
-    n = ((2 if fused_refresh else 3) - (1 if ranked_in_decode else 0) if spec.top_k is not None else 0) + 1 + \
-        (0 if fold else 1)
+    # ... and scored there too when each CTA's share of a full row fits its
+    # staging memory at once (fused_score_pages_per_round in decode.cu)
+    ring = (spec.head_dim // 64) * 16 * 128 * 2 * (1 if spec.head_dim == 128 else 2) * 2 * 6
+    per_round = ring // (16 * (4 * spec.head_dim + 4)) * 16
+    scored_in_decode = ranked_in_decode and k >= 2 and -(-inputs["page_table"].shape[1] // k) <= per_round
+    n = ((2 if fused_refresh else 3) - (1 if ranked_in_decode else 0) - (1 if scored_in_decode else 0)
+         if spec.top_k is not None else 0) + 1 + (0 if fold else 1)
     return n + (1 if prefix else 0)
 
 

@@ -248,6 +248,107 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
     }
 }
 
+// Fused scoring (TinyServe query-aware page selection, s2.2-2.3: the bound
+// score of every page from its metadata; s5.3: the last page's metadata is
+// recomputed first).  Block `blk` of the k CTAs of row `row` scores the
+// row's 16-page groups [blk ng / k, (blk + 1) ng / k).  `stage` (stage_bytes
+// of shared memory) takes the page ids and metadata rows of as many groups
+// at a time as fit (the host takes this path only when one round covers a
+// CTA's share): the ids first (one coalesced pass), then the rows by
+// 16-byte copies through L2 (consecutive threads copy consecutive chunks of
+// a row; chunk c of slot s sits at c ^ (s & 7), so the eight rows one
+// fragment load touches fall in different banks); each warp then scores
+// whole groups with bound_group_scores (the scoring kernel's product, in the
+// same order: equal bits) and stores them to the row's scores.  The last
+// page's new metadata is written before the CTA barrier that precedes the
+// copies (which are plain loads into shared memory, ordered by it).
+template <int D, bool QF32, int WPC>
+__device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, int seq, int n_b, uint8_t *stage,
+                                size_t stage_bytes, const int32_t *pt_row, const void *s_q) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    constexpr int ROWB = 4 * D;        // bytes of one bf16 metadata row [m | M]
+    constexpr int CPRW = ROWB / 16;    // its 16-byte chunks
+    constexpr int NT = WPC * 32;
+    const int cap_groups = int(stage_bytes / (16 * (ROWB + 4)));
+    int32_t *s_ids = reinterpret_cast<int32_t *>(stage + size_t(cap_groups) * 16 * ROWB);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3, gid = lane >> 2;
+    const int g = row % a.num_kv_heads;
+    const int ng = (n_b + 15) >> 4;
+    const int g0 = int(int64_t(blk) * ng / k), g1 = int(int64_t(blk + 1) * ng / k);
+    const char *meta = static_cast<const char *>(a.meta);
+    const int fresh_j = a.refresh && n_b > 0 ? n_b - 1 : -1;
+    if (fresh_j >= 0 && blk == k - 1 && warp == 0) {  // the CTA holding the last group
+        const int p = pt_row[fresh_j];
+        if (p >= 0 && p < a.num_pool_pages)  // a bad id is flagged by the scan below
+            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, p, g, seq - fresh_j * a.page_size, a.num_kv_heads,
+                                            a.page_size);
+    }
+    if (!(a.top_k < n_b || a.score_all)) return;  // CTA-uniform: every page is kept, no score asked for
+    __syncthreads();  // the refreshed row, before another warp reads it
+
+    uint32_t bh[NKP][4], bl[NKP][4];
+    {
+        uint4 qraw[NKP][QF32 ? 2 : 1];
+        const bool head_ok = gid < a.group;
+        const uint8_t *qh = static_cast<const uint8_t *>(s_q) + (head_ok ? gid : 0) * D * (QF32 ? 4 : 2);
+#pragma unroll
+        for (int kp = 0; kp < NKP; kp++) {
+            const int col = bound_q_col<D>(4 * kp + t);
+            if (QF32) {
+                qraw[kp][0] = *reinterpret_cast<const uint4 *>(qh + col * 4);
+                qraw[kp][QF32 ? 1 : 0] = *reinterpret_cast<const uint4 *>(qh + col * 4 + 16);
+            } else {
+                qraw[kp][0] = *reinterpret_cast<const uint4 *>(qh + col * 2);
+            }
+        }
+        bound_q_operand<D, QF32>(qraw, head_ok, bh, bl);
+    }
+    float *srow = a.scores + int64_t(row) * a.max_pages;
+    const float NEG = -INFINITY;
+    for (int rg = g0; rg < g1; rg += cap_groups) {
+        const int ngr = min(cap_groups, g1 - rg);
+        const int j0 = rg * 16;
+        for (int sl = threadIdx.x; sl < ngr * 16; sl += NT) s_ids[sl] = j0 + sl < n_b ? pt_row[j0 + sl] : -1;
+        __syncthreads();
+        for (int i = threadIdx.x; i < ngr * 16 * CPRW; i += NT) {
+            const int sl = i / CPRW, c = i % CPRW;
+            const int j = j0 + sl;
+            if (j < n_b) {
+                const int p = s_ids[sl];
+                if (p >= 0 && p < a.num_pool_pages)
+                    cp_async_cg16(stage + sl * ROWB + ((c ^ (sl & 7)) << 4),
+                                  meta + (int64_t(p) * a.num_kv_heads + g) * ROWB + c * 16);
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        for (int gi = warp; gi < ngr; gi += WPC) {
+            const int sa_ = gi * 16 + gid, sb_ = sa_ + 8;  // both = gid (mod 8)
+            const int ja = j0 + sa_, jb = j0 + sb_;
+            const bool va = ja < n_b, vb = jb < n_b;
+            const int pa = va ? s_ids[sa_] : 0, pb = vb ? s_ids[sb_] : 0;
+            const bool bada = va && (pa < 0 || pa >= a.num_pool_pages);
+            const bool badb = vb && (pb < 0 || pb >= a.num_pool_pages);
+            if ((bada || badb) && t == 0) raise_error(a.flags, kErrPageId);
+            uint4 xa[NKP], xb[NKP];
+#pragma unroll
+            for (int kp = 0; kp < NKP; kp++) {
+                const int c = 4 * kp + t;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                xa[kp] = va && !bada ? *reinterpret_cast<const uint4 *>(stage + sa_ * ROWB + ((c ^ gid) << 4)) : z;
+                xb[kp] = vb && !badb ? *reinterpret_cast<const uint4 *>(stage + sb_ * ROWB + ((c ^ gid) << 4)) : z;
+            }
+            float sa, sb;
+            bound_group_scores<D, QF32>(xa, xb, bh, bl, a.group, sa, sb);
+            if (t == 0) {
+                if (va) srow[ja] = bada ? NEG : sa;
+                if (vb) srow[jb] = badb ? NEG : sb;
+            }
+        }
+        __syncthreads();  // the stage is read, before the next round (or the ranking) reuses it
+    }
+}
+
 // A stage holds up to HALVES 16-token sub-tiles ("halves") of one row: K
 // then V, each half as D/64 boxes of 16 tokens x 64 dims (128-byte swizzle).
 // HINT: the call streams more K/V than L2 holds; the loads carry an
@@ -264,7 +365,7 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // with k > 1 into one piece per block in the workspace, and the block that
 // draws the row's last ticket (a per-row counter; no block waits for
 // another) folds the k pieces with all its threads and resets the counter.
-template <int D, bool QF32, int WPC, int HALVES, bool HINT, bool ROWCTA, bool RANK = false>
+template <int D, bool QF32, int WPC, int HALVES, bool HINT, bool ROWCTA, bool RANK = false, bool SCORE = false>
 __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        DecodeArgs a) {
@@ -325,6 +426,8 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                               D * (QF32 ? 4 : 2));
         for (int i = threadIdx.x; i < G * QV; i += WPC * 32) s_q[i] = qg[i];
     }
+    // the row's sequence length (an input too), for the fused rank / score
+    const int rc_seq = ROWCTA && RANK ? __ldg(a.seq_lens + rc_row / a.num_kv_heads) : 0;
     if (!a.wait_at_exit) pdl_wait();
     if constexpr (ROWCTA) {
         __syncthreads();
@@ -342,10 +445,21 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             sa.need_max = 0;
             sa.seed = 0;
             const int b = rc_row / a.num_kv_heads;
-            int seq = __ldg(a.seq_lens + b);
+            int seq = rc_seq;
             const int cap = a.max_pages * a.page_size;
-            seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
+            if (SCORE && (seq < 0 || seq > cap) && threadIdx.x == 0 && rc_blk == 0) raise_error(a.flags, kErrSeqLen);
+            seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel (or above)
             const int n_b = (seq + a.page_size - 1) / a.page_size;
+            if constexpr (SCORE) {
+                // the CTA's share of the row's scores, staged through the
+                // rings' memory; then every CTA of the row (cluster) sees all
+                score_row_share<D, QF32, WPC>(a, rc_row, rc_blk, rc_k, seq, n_b, ring0, size_t(WPC) * S * STAGE,
+                                              a.pt_in_smem ? s_pt : a.page_table + int64_t(b) * a.max_pages, s_q);
+                if (rc_k > 1)
+                    cluster_sync();
+                else
+                    __syncthreads();
+            }
             const int nsel = select_row<WPC * 32>(sa, rc_row, n_b, a.scores + int64_t(rc_row) * a.max_pages, sm,
                                                   s_code, rc_blk == 0);
             fence_proxy_async_smem();  // the keys' stores, before TMA refills of the same memory
@@ -968,7 +1082,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeArgs a) {
     if (cur_row >= 0) finish_row(cur_row);
 }
 
-template <int D, bool QF32, bool HINT, bool ROWCTA, bool RANK = false>
+template <int D, bool QF32, bool HINT, bool ROWCTA, bool RANK = false, bool SCORE = false>
 cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                              const DecodeGrid &grid, cudaStream_t stream) {
     constexpr int WPC = D == 128 ? kDecodeWarpsD128 : kDecodeWarpsD64;
@@ -977,7 +1091,7 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     // ROWCTA: the row's unit codes after the rings, then its page-table row if staged
     const size_t smem = decode_smem_bytes(D, a.stages) + (ROWCTA ? rowcta_extra_smem(a, D * (QF32 ? 4 : 2)) : 0);
     const unsigned ctas = ROWCTA ? unsigned(int64_t(a.batch) * a.num_kv_heads * a.row_blocks) : unsigned(grid.ctas);
-    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA, RANK>;
+    auto kernel = decode_bf16_kernel<D, QF32, WPC, HALVES, HINT, ROWCTA, RANK, SCORE>;
     static size_t configured[64] = {0};  // dynamic smem limit already set, per device
     static std::mutex mu;                // calls may come from several host threads
     int dev = 0;
@@ -990,12 +1104,18 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
             if (dev >= 0 && dev < 64) configured[dev] = smem;
         }
     }
-    return launch_pdl(kernel, dim3(ctas), dim3(WPC * 32), smem, stream, *tk, *tv, a);
+    // the fused scoring shares a row's scores among its k CTAs: one cluster
+    const unsigned cluster = SCORE && ROWCTA ? unsigned(a.row_blocks) : 1u;
+    if (cluster > unsigned(kRowBlocksMax)) return cudaErrorInvalidConfiguration;
+    return launch_pdl_cluster(kernel, dim3(ctas), dim3(WPC * 32), smem, stream, cluster, *tk, *tv, a);
 }
 
 template <int D, bool QF32>
 cudaError_t launch_bf16(const DecodeArgs &a, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeGrid &grid,
                         cudaStream_t stream, bool rowcta = false) {
+    if (rowcta && a.scores && a.meta)  // fused score + rank + decode
+        return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true, true, true>(a, tk, tv, grid, stream)
+                                : launch_bf16_hint<D, QF32, false, true, true, true>(a, tk, tv, grid, stream);
     if (rowcta && a.scores)  // fused rank + decode
         return a.kv_evict_first ? launch_bf16_hint<D, QF32, true, true, true>(a, tk, tv, grid, stream)
                                 : launch_bf16_hint<D, QF32, false, true, true>(a, tk, tv, grid, stream);
@@ -1032,6 +1152,13 @@ cudaError_t noalloc_scratch_address(void **ptr) {
     return cudaSuccess;
 }
 
+int fused_score_pages_per_round(int head_dim) {
+    // the rings' memory holds the page ids and bf16 metadata rows (4 d bytes)
+    // of whole 16-page groups (score_row_share)
+    const size_t ring = decode_smem_bytes(head_dim, decode_stages(head_dim)) - 1024;
+    return int(ring / (16 * (size_t(4) * head_dim + 4))) * 16;
+}
+
 size_t rowcta_extra_smem(const DecodeArgs &a, int q_bytes) {
     return size_t((a.slots_per_row + 3) & ~3) * 4 + (a.pt_in_smem ? size_t((a.max_pages + 3) & ~3) * 4 : 0) +
            size_t(a.group) * q_bytes;
@@ -1050,7 +1177,7 @@ int row_blocks_for(int64_t rows, int slots_per_row, int ctas, bool no_extra_piec
 
 size_t rowcta_smem_budget() {
     // dynamic shared memory per CTA with kDecodeCtasPerSm CTAs per SM (less
-    // a margin for the kernel's static shared memory), cached per device
+    // a margin for the kernel's static shared memory, about 2 KB), cached per device
     static size_t budget[64] = {0};
     static std::mutex mu;
     int dev = 0;
@@ -1061,7 +1188,7 @@ size_t rowcta_smem_budget() {
         if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return 0;
-        const int64_t b = int64_t(per_sm) / kDecodeCtasPerSm - reserved - 2048;
+        const int64_t b = int64_t(per_sm) / kDecodeCtasPerSm - reserved - 3072;
         budget[dev] = b > 0 ? size_t(b) : 1;
     }
     return budget[dev];

@@ -83,13 +83,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(SelectArgs a) {
 
 // ---------------------------------------------- scores on tensor cores --
 // One warp scores 32 pages of a row: two groups of 16 pages, each a
-// (16 pages x 2D) . (2D x 8 heads) mma.sync product.  Lane (gid, t) loads
-// 16-byte chunks 4 kp + t (kp < NKP) of the metadata rows of pages gid and
-// gid + 8 of both groups, and the matching chunks of head gid's query.
-template <int D>
-struct BoundScanRegs {
-    static constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
-};
+// (16 pages x 2D) . (2D x 8 heads) mma.sync product (bound_group_scores).
 
 // Query chunks of head `gid` of KV head g's group (zero past the group).
 template <int D, bool QF32>
@@ -100,8 +94,7 @@ __device__ __forceinline__ void bound_load_q(const SelectArgs &a, int b, int g, 
     const int64_t qoff = (int64_t(b) * a.num_q_heads + int64_t(g) * a.group + (head_ok ? gid : 0)) * D;
 #pragma unroll
     for (int kp = 0; kp < NKP; kp++) {
-        const int c = 4 * kp + t;
-        const int col = 8 * c - (8 * c >= D ? D : 0);
+        const int col = bound_q_col<D>(4 * kp + t);
         if (QF32) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + qoff + col);
             qraw[kp][0] = qp[0];
@@ -164,68 +157,15 @@ __device__ __forceinline__ void bound_score_store(const SelectArgs &a, const uin
                                                   float *srow) {
     constexpr int NKP = BoundScanRegs<D>::NKP;
     const int lane = threadIdx.x & 31, t = lane & 3, gid = lane >> 2;
-    const bool head_ok = gid < a.group;
-    // B operand: the [q- | q+] column of head gid of the group, in the chunk
-    // order this lane uses for the metadata rows.
     uint32_t bh[NKP][4], bl[NKP][4];
-#pragma unroll
-    for (int kp = 0; kp < NKP; kp++) {
-        const bool upper = 8 * (4 * kp + t) >= D;  // chunk of the M half: pairs with q+
-        float v[8];
-        if (QF32) {
-            const uint4 x0 = qraw[kp][0], x1 = qraw[kp][QF32 ? 1 : 0];
-            v[0] = __uint_as_float(x0.x); v[1] = __uint_as_float(x0.y);
-            v[2] = __uint_as_float(x0.z); v[3] = __uint_as_float(x0.w);
-            v[4] = __uint_as_float(x1.x); v[5] = __uint_as_float(x1.y);
-            v[6] = __uint_as_float(x1.z); v[7] = __uint_as_float(x1.w);
-        } else {
-            const uint4 x = qraw[kp][0];
-            v[0] = bf16_lo_to_float(x.x); v[1] = bf16_hi_to_float(x.x);
-            v[2] = bf16_lo_to_float(x.y); v[3] = bf16_hi_to_float(x.y);
-            v[4] = bf16_lo_to_float(x.z); v[5] = bf16_hi_to_float(x.z);
-            v[6] = bf16_lo_to_float(x.w); v[7] = bf16_hi_to_float(x.w);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            v[i] = upper ? fmaxf(v[i], 0.f) : fminf(v[i], 0.f);
-            if (!head_ok) v[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            bh[kp][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-            if (QF32) {
-                const float r0 = v[2 * i] - bf16_lo_to_float(bh[kp][i]);
-                const float r1 = v[2 * i + 1] - bf16_hi_to_float(bh[kp][i]);
-                bl[kp][i] = pack_bf16x2(r0, r1);
-            }
-        }
-    }
-
+    bound_q_operand<D, QF32>(qraw, gid < a.group, bh, bl);
     const float NEG = -INFINITY;
-    const bool h0 = 2 * t < a.group, h1 = 2 * t + 1 < a.group;
 #pragma unroll
     for (int grp = 0; grp < 2; grp++) {
         const int ia = 2 * grp, ib = 2 * grp + 1;
         if (w_page0 + grp * 16 >= n_b) break;  // warp-uniform: the group holds no page
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kp = 0; kp < NKP; kp++) {
-            const uint32_t fa0[4] = {av[ia][kp].x, av[ib][kp].x, av[ia][kp].y, av[ib][kp].y};
-            const uint32_t fa1[4] = {av[ia][kp].z, av[ib][kp].z, av[ia][kp].w, av[ib][kp].w};
-            mma_bf16_16816(acc, fa0, bh[kp][0], bh[kp][1]);
-            mma_bf16_16816(acc, fa1, bh[kp][2], bh[kp][3]);
-            if (QF32) {
-                mma_bf16_16816(acc, fa0, bl[kp][0], bl[kp][1]);
-                mma_bf16_16816(acc, fa1, bl[kp][2], bl[kp][3]);
-            }
-        }
-        // acc: [page gid][head 2t], [gid][2t+1], [gid+8][2t], [gid+8][2t+1]
-        float sa = fmaxf(h0 ? acc[0] : NEG, h1 ? acc[1] : NEG);
-        float sb = fmaxf(h0 ? acc[2] : NEG, h1 ? acc[3] : NEG);
-        sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 1));
-        sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 2));
-        sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 1));
-        sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 2));
+        float sa, sb;
+        bound_group_scores<D, QF32>(av[ia], av[ib], bh, bl, a.group, sa, sb);
         if (t == 0) {
             if (vv[ia]) srow[jj[ia]] = bad[ia] ? NEG : sa;
             if (vv[ib]) srow[jj[ib]] = bad[ib] ? NEG : sb;

@@ -496,8 +496,15 @@ qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float *sc = scores ? scores : reinterpret_cast<float *>(ws + L.scores);
     uint32_t *tickets = reinterpret_cast<uint32_t *>(ws + L.tickets);
-    // the decode ranks its own rows when they go one row per k CTAs
-    const bool fused = row_blocks_for(rows, top_k, grid.ctas, true, true) > 0;
+    // The decode ranks its own rows when they go one row per k CTAs.  With
+    // k >= 2, when each CTA's share of a full row's pages (max_pages / k)
+    // fits its staging memory at once, it also scores them (the k CTAs of a
+    // row one cluster) and the step is that one launch; longer shares would
+    // be staged in serial rounds, slower than the scoring grid (measured).
+    const int rk = row_blocks_for(rows, top_k, grid.ctas, true, true);
+    const bool fused = rk > 0;
+    const bool fused_score = rk >= kFusedScoreMinBlocks &&
+                             (int64_t(shape->max_pages) + rk - 1) / rk <= fused_score_pages_per_round(shape->head_dim);
 
     SelectArgs sa;
     sa.k_pool = k_pool;
@@ -522,9 +529,10 @@ qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_
     sa.seed = 0;
     sa.meta_evict_first = 0;
     sa.head_quads = 0;
-    QSKV_TRY(launched(launch_page_select(sa, q_dtype, QSKV_BF16, shape->head_dim, st, scores != nullptr, 1,
-                                         fused ? 0 : 1),
-                      "select_decode scoring launch"));
+    if (!fused_score)
+        QSKV_TRY(launched(launch_page_select(sa, q_dtype, QSKV_BF16, shape->head_dim, st, scores != nullptr, 1,
+                                             fused ? 0 : 1),
+                          "select_decode scoring launch"));
 
     DecodeArgs a;
     a.q = q;
@@ -564,6 +572,12 @@ qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_
         a.scores = sc;
         a.selected_out = selected;
         a.n_selected_out = n_selected;
+    }
+    if (fused_score) {
+        a.meta = meta;
+        a.meta_w = meta;
+        a.refresh = 1;
+        a.score_all = scores != nullptr ? 1 : 0;
     }
     CUtensorMap tk, tv;
     QSKV_TRY(make_pool_map(&tk, k_pool, shape));

@@ -88,6 +88,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (not L1), and the
+// wait for every copy this thread issued.
+__device__ __forceinline__ void cp_async_cg16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Barrier over every thread of the thread-block cluster: the release /
+// acquire pair makes each CTA's earlier memory writes (global included)
+// visible to the other CTAs of the cluster after it.  All threads of every
+// CTA of the cluster execute it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch --
 // Every kernel is launched with programmatic stream serialization, so it may
 // start while the previous kernel in the stream drains.  pdl_wait() blocks
@@ -113,6 +130,30 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// launch_pdl with the CTAs grouped into thread-block clusters of
+// `cluster` consecutive blocks (1: no cluster).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t stream, unsigned cluster, Args... args) {
+    if (cluster <= 1) return launch_pdl(kernel, grid, block, smem, stream, args...);
+    if (grid.x % cluster != 0) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 #endif
@@ -504,9 +545,18 @@ struct DecodeArgs {
     // Fused rank + decode (one row per k CTAs): each CTA first ranks its row's
     // `scores` (top_k, exact) itself; block 0 of the row writes the list and
     // count to selected_out / n_selected_out.
-    const float *scores = nullptr;
+    float *scores = nullptr;
     int32_t *selected_out = nullptr;
     int32_t *n_selected_out = nullptr;
+    // Fused score + rank + decode (one row per k CTAs, the k CTAs of a row
+    // one thread-block cluster): each CTA first scores its share of the
+    // row's pages from `meta` into `scores` (all rows when score_all, else
+    // only rows with more pages than top_k), after the last CTA of the row
+    // has recomputed the last page's metadata into meta_w when `refresh`.
+    const void *meta = nullptr;
+    void *meta_w = nullptr;
+    int32_t refresh = 0;
+    int32_t score_all = 0;
 };
 
 // Shared-prefix cascade: the attention of all B x G query rows of one KV head
@@ -587,6 +637,13 @@ constexpr int kMaxStages = 8;
 // (their pieces are folded with one round of loads).
 constexpr int kRowCtaMaxSlots = 1024;
 constexpr int kRowBlocksMax = 8;
+// One-call steps (bf16 KV, exact top-K): rows split over at least this many
+// decode CTAs are scored by those CTAs themselves (one cluster per row)
+// instead of by the scoring grid.
+#ifndef QSKV_FUSED_SCORE_MIN_BLOCKS
+#define QSKV_FUSED_SCORE_MIN_BLOCKS 2
+#endif
+constexpr int kFusedScoreMinBlocks = QSKV_FUSED_SCORE_MIN_BLOCKS;
 // The decode grid folds a split row itself when one warp can load all of the
 // row's pieces in a single round of at most this many 16-byte loads per lane
 // (pieces x G x D / 128).  Measured on GB300: the GPT2-like rows (15 pieces

@@ -89,5 +89,7 @@ size_t rowcta_smem_budget();
 int decode_stages(int head_dim);
 int decode_warps_per_cta(int head_dim);
 size_t decode_smem_bytes(int head_dim, int stages);
+// Pages one decode CTA can stage for the fused scoring in one round.
+int fused_score_pages_per_round(int head_dim);
 
 }  // namespace qskv

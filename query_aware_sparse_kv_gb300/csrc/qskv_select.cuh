@@ -1,7 +1,9 @@
 // Ranking of one row's page scores by one CTA (the top-K select of
-// TinyServe query-aware page selection, s2.3: "radix sort in shared memory"),
+// TinyServe query-aware page selection, s2.3: radix sort in shared memory),
 // shared by the ranking kernel (page_select.cu) and the fused rank + decode
-// launch (decode.cu).  MSB-first radix select over 8-bit digits of
+// launch (decode.cu); and the bound product of s2.2 on the tensor cores,
+// shared by the scoring kernel and the decode launch that scores its own
+// rows.  MSB-first radix select over 8-bit digits of
 // order-preserving 32-bit keys, stopping early when a bucket is taken whole;
 // stable compaction in page order (ties to the lower page index); the lossy
 // variant of the Vortex digest (method overview item 3) when a.need_max > 0.
@@ -19,6 +21,115 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 __device__ __forceinline__ uint32_t shr32(uint32_t x, int s) { return s >= 32 ? 0u : (x >> s); }
+
+// ---------------------------------------------------------- bound score --
+// With q- = min(q, 0) and q+ = max(q, 0) the bound of page j is the dot
+// product [m_j | M_j] . [q- | q+].  The scores of 16 pages for the G <= 8
+// heads of a group are a (16 pages x 2D) . (2D x 8 heads) m16n8k16 bf16
+// product with fp32 accumulation.  Lane (gid, t) holds the 16-byte chunks
+// 4 kp + t (kp < NKP) of the metadata rows of pages gid and gid + 8 (the A
+// operand) and the same chunks of head gid's [q- | q+] column (the B
+// operand): A and B use one permutation of the 2D-long k axis, which the dot
+// product does not see.  bf16 products are exact in fp32; fp32 queries are
+// split into hi + lo bf16 halves (two mma per k-step).
+template <int D>
+struct BoundScanRegs {
+    static constexpr int NKP = 2 * D / 32;  // 16-byte chunks per lane per metadata row
+};
+
+// Column of the 2D-long k axis where this lane's chunk c starts in q: the
+// first D columns pair m with q-, the next D pair M with q+.
+template <int D>
+__device__ __forceinline__ int bound_q_col(int c) { return 8 * c - (8 * c >= D ? D : 0); }
+
+// B operand (bh, and the lo halves bl for fp32 q) from the lane's raw query
+// chunks qraw[kp] (chunk 4 kp + t of head gid; 8 floats or 8 bf16).
+template <int D, bool QF32>
+__device__ __forceinline__ void bound_q_operand(const uint4 (&qraw)[2 * D / 32][QF32 ? 2 : 1], bool head_ok,
+                                                uint32_t (&bh)[2 * D / 32][4], uint32_t (&bl)[2 * D / 32][4]) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    const int t = threadIdx.x & 3;
+#pragma unroll
+    for (int kp = 0; kp < NKP; kp++) {
+        const bool upper = 8 * (4 * kp + t) >= D;  // chunk of the M half: pairs with q+
+        float v[8];
+        if (QF32) {
+            const uint4 x0 = qraw[kp][0], x1 = qraw[kp][QF32 ? 1 : 0];
+            v[0] = __uint_as_float(x0.x); v[1] = __uint_as_float(x0.y);
+            v[2] = __uint_as_float(x0.z); v[3] = __uint_as_float(x0.w);
+            v[4] = __uint_as_float(x1.x); v[5] = __uint_as_float(x1.y);
+            v[6] = __uint_as_float(x1.z); v[7] = __uint_as_float(x1.w);
+        } else {
+            const uint4 x = qraw[kp][0];
+            v[0] = bf16_lo_to_float(x.x); v[1] = bf16_hi_to_float(x.x);
+            v[2] = bf16_lo_to_float(x.y); v[3] = bf16_hi_to_float(x.y);
+            v[4] = bf16_lo_to_float(x.z); v[5] = bf16_hi_to_float(x.z);
+            v[6] = bf16_lo_to_float(x.w); v[7] = bf16_hi_to_float(x.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            v[i] = upper ? fmaxf(v[i], 0.f) : fminf(v[i], 0.f);
+            if (!head_ok) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            bh[kp][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            if (QF32) {
+                const float r0 = v[2 * i] - bf16_lo_to_float(bh[kp][i]);
+                const float r1 = v[2 * i + 1] - bf16_hi_to_float(bh[kp][i]);
+                bl[kp][i] = pack_bf16x2(r0, r1);
+            }
+        }
+    }
+}
+
+// Row scores of one 16-page group: xa / xb are the lane's chunks of the
+// metadata rows of pages gid and gid + 8.  Returns in sa / sb the best head's
+// bound of those two pages (valid in the lanes with t = 0).  The k axis is
+// summed in four independent accumulator chains (kp even / odd x the two
+// halves of a chunk), issued round-robin so consecutive mma do not wait on
+// each other, then added pairwise.  Every caller accumulates in this one
+// order, so the two scoring paths give equal bits.
+template <int D, bool QF32>
+__device__ __forceinline__ void bound_group_scores(const uint4 (&xa)[2 * D / 32], const uint4 (&xb)[2 * D / 32],
+                                                   const uint32_t (&bh)[2 * D / 32][4],
+                                                   const uint32_t (&bl)[2 * D / 32][4], int group, float &sa,
+                                                   float &sb) {
+    constexpr int NKP = BoundScanRegs<D>::NKP;
+    static_assert(NKP % 2 == 0, "chunks come in pairs");
+    const int t = threadIdx.x & 3;
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kp = 0; kp < NKP; kp += 2) {
+        const uint32_t a0[4] = {xa[kp].x, xb[kp].x, xa[kp].y, xb[kp].y};
+        const uint32_t a1[4] = {xa[kp].z, xb[kp].z, xa[kp].w, xb[kp].w};
+        const uint32_t a2[4] = {xa[kp + 1].x, xb[kp + 1].x, xa[kp + 1].y, xb[kp + 1].y};
+        const uint32_t a3[4] = {xa[kp + 1].z, xb[kp + 1].z, xa[kp + 1].w, xb[kp + 1].w};
+        mma_bf16_16816(c0, a0, bh[kp][0], bh[kp][1]);
+        mma_bf16_16816(c1, a1, bh[kp][2], bh[kp][3]);
+        mma_bf16_16816(c2, a2, bh[kp + 1][0], bh[kp + 1][1]);
+        mma_bf16_16816(c3, a3, bh[kp + 1][2], bh[kp + 1][3]);
+        if (QF32) {
+            mma_bf16_16816(c0, a0, bl[kp][0], bl[kp][1]);
+            mma_bf16_16816(c1, a1, bl[kp][2], bl[kp][3]);
+            mma_bf16_16816(c2, a2, bl[kp + 1][0], bl[kp + 1][1]);
+            mma_bf16_16816(c3, a3, bl[kp + 1][2], bl[kp + 1][3]);
+        }
+    }
+    float acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) acc[i] = (c0[i] + c2[i]) + (c1[i] + c3[i]);
+    // acc: [page gid][head 2t], [gid][2t+1], [gid+8][2t], [gid+8][2t+1]
+    const float NEG = -INFINITY;
+    const bool h0 = 2 * t < group, h1 = 2 * t + 1 < group;
+    sa = fmaxf(h0 ? acc[0] : NEG, h1 ? acc[1] : NEG);
+    sb = fmaxf(h0 ? acc[2] : NEG, h1 ? acc[3] : NEG);
+    sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 1));
+    sa = fmaxf(sa, __shfl_xor_sync(0xffffffffu, sa, 2));
+    sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 1));
+    sb = fmaxf(sb, __shfl_xor_sync(0xffffffffu, sb, 2));
+}
 
 // --------------------------------------------------------------- select --
 // Exclusive block scans of x and y; total_y gets the sum of y over the block.

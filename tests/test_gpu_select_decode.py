@@ -5,10 +5,16 @@ refreshed every step), s2.1-2.3 (min/max metadata, bound score, top-K) and
 s3.2 (attention over the selected pages only).  The call is the scoring
 launch (with the last-page refresh inside) followed by the decode launch;
 when the rows go one row per k decode CTAs, the decode CTAs rank their own
-row's scores before they stream its pages (no ranking launch).
+row's scores before they stream its pages (no ranking launch), and with
+k >= 2, when a CTA's share of a full row's pages fits its staging memory at
+once, they also score the row themselves, the k CTAs of a row forming one
+thread-block cluster (the step is one launch).
 
-Checked, on cases with k = 1, k = 2, k = 8 and a batch too large for that
-split (the ranking launch runs): the refreshed metadata bit for bit against
+Checked, on cases with k = 1, k = 2, k = 4 and k = 8 scored in the decode
+launch (d = 64 with fp32 q, d = 128 with bf16 q), k = 8 with shares too
+long for that (the scoring launch runs; d = 64 and d = 128), k = 1 and a
+batch too large for the split (the ranking launch runs): the refreshed
+metadata bit for bit against
 the oracle's scan of the new keys, scores and selections against the
 oracle's, outputs against the oracle's attention over the selected pages,
 and every result (metadata, scores, selection, out, lse) equal bit for bit
@@ -58,6 +64,13 @@ def _case(kind):
         return W.spec_for("gpt2_345m")
     if kind == "long_k8":    # 24 rows of 32-token pages
         return W.spec_for("long_context", batch=3, seq_len_range=(3000, 9000), max_pages=None, top_k=64)
+    if kind == "long_rounds_k8":  # the long-context batch: 256-512 pages per CTA, d = 128
+        return W.spec_for("long_context")
+    if kind == "gpt2_rounds_k8":  # 32 MHA rows of 4096 pages: 512 per CTA, d = 64, fp32 q
+        return W.spec_for("gpt2_345m", batch=2, seq_lens=(65536, 61000))
+    if kind == "edges_k4":   # 64 rows of no, one, two and many pages, split over 4 CTAs each
+        return W.spec_for("llama3_8b", batch=8, seq_lens=(0, 1, 15, 16, 17, 33, 3000, 5000), seq_len_range=None,
+                          max_pages=None, top_k=64, kind="iid")
     if kind == "edges_k1":   # rows of no, one, two and many pages
         batch = -(-sms // 8) + 1
         lens = [0, 1, 15, 16, 17, 33] + [3000 + 97 * i for i in range(batch - 6)]
@@ -85,13 +98,17 @@ def _nan_like(t):
     return torch.full_like(t, float("nan"))
 
 
-@pytest.mark.parametrize("kind", ["llama_k1", "gpt2_k2", "long_k8", "edges_k1", "many_rows"])
+KINDS = {"llama_k1": 1, "gpt2_k2": 2, "long_k8": 8, "long_rounds_k8": 8, "gpt2_rounds_k8": 8, "edges_k1": 1,
+         "edges_k4": 4, "many_rows": 0}
+
+
+@pytest.mark.parametrize("kind", list(KINDS))
 def test_select_decode_matches_the_oracle_and_the_separate_calls(oracle_lib, kind):
     spec = _case(kind)
     inp = W.make_inputs(spec)
     rows = spec.batch * spec.num_kv_heads
     k = row_blocks(rows, spec.top_k, _sms())
-    want = {"llama_k1": 1, "gpt2_k2": 2, "long_k8": 8, "edges_k1": 1, "many_rows": 0}[kind]
+    want = KINDS[kind]
     assert k == want, f"unexpected split (k = {k})"
     ids, vt = oracle_lib.all_pages(inp)
     old_meta = oracle_lib.meta(inp["k_pool"], ids, vt)
@@ -113,10 +130,10 @@ def test_select_decode_matches_the_oracle_and_the_separate_calls(oracle_lib, kin
     new_meta = oracle_lib.meta(inp["k_pool"], last_ids, last_valid, out=old_meta.copy())
     PR.assert_meta_equal(dec.meta, new_meta, ids)
     check = list(range(rows)) if rows <= 256 else PR.sample_rows(rows, 96, seed=5)
-    if kind == "edges_k1":
+    if kind.startswith("edges"):
         check = [r for r in check if r >= spec.num_kv_heads]
     PR.check_rows(inp, dec, check, oracle_lib, oracle_meta=new_meta, check_scores=sc)
-    if kind == "edges_k1":  # the sequence with no token: nothing selected, output 0, lse -inf
+    if kind.startswith("edges"):  # the sequence with no token: nothing selected, output 0, lse -inf
         assert (dec.n_selected[0] == 0).all()
         assert (dec.out[0] == 0).all() and torch.isneginf(dec.lse[0]).all()
 
