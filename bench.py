@@ -2,9 +2,10 @@
 
 A step is one pass of the whole hot path over one batch: refresh the
 metadata of the page each sequence appends to, select the top-K pages per
-(sequence, KV head), and run sparse paged decode over them (two library
-calls: the refresh runs inside the scoring launch; scoring, ranking, decode
-and, where the decode does not fold its split rows itself, a merge).  Inputs are synthetic and resident in HBM.  The
+(sequence, KV head), and run sparse paged decode over them (one library
+call, qskv_select_decode, for the bf16 workloads with a top-K: one to three
+launches by shape; the dense shared-prefix batch is the cascade decode alone;
+the fp32 tiny batch takes the separate calls).  Inputs are synthetic and resident in HBM.  The
 query rotates over 16 variants, and where one step's K/V would fit in a few
 L2s the steps also rotate over copies of the KV pool and its metadata, so
 that a step never finds its K/V in the 129 MB L2.
@@ -398,7 +399,7 @@ def source_hash(paths) -> str:
 
 
 DECODE_SOURCES = [os.path.join(ROOT, "query_aware_sparse_kv_gb300", "csrc", n)
-                  for n in ("decode.cu", "merge.cu", "qskv_device.cuh", "qskv_internal.h")]
+                  for n in ("decode.cu", "merge.cu", "qskv_device.cuh", "qskv_internal.h", "qskv_select.cuh")]
 
 
 def ncu_traffic(workload: str):
@@ -524,8 +525,7 @@ class Bench:
     @property
     def one_call(self) -> bool:
         """Whether a step is PagedDecoder.step's single call (qskv_select_decode:
-        scoring with the last-page refresh, then the decode, which ranks its own
-        rows when they go one row per k CTAs)."""
+        one to three launches by shape)."""
         return (self.spec.top_k is not None and self.dec.can_refresh_in_select
                 and not self.args.separate_calls)
 
@@ -887,7 +887,8 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "recall": recall,
         "step_launch": ("CUDA graph replay, one graph per query variant: " +
-                        ("qskv_select_decode (scoring launch with the last-page metadata refresh inside, then the "
+                        ("qskv_select_decode (one launch where the decode CTAs of a row also refresh and score "
+                         "it; else the scoring launch with the last-page metadata refresh inside, then the "
                          "decode launch, which ranks its own rows when they go one row per k CTAs)" if main.one_call
                          else "scoring (last-page metadata refresh inside where it can be) + ranking + decode")
                         if spec.top_k is not None else

@@ -10,7 +10,9 @@
  *
  * (qskv_page_select_refresh does the first two in one launch: the last
  * pages' metadata refresh inside the scoring grid; qskv_select_decode does
- * the whole step in one call, two launches),
+ * the whole step in one call: one launch when the rows fit one wave of
+ * decode CTAs and a CTA's share of a row's metadata fits its shared memory,
+ * else two or three),
  *
  * with an alternative block score (the mean key of each page, "Block Top-K"):
  *
@@ -289,10 +291,18 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
  * n_selected, scores) followed by qskv_sparse_paged_decode(q, k_pool,
  * v_pool, ..., selected, n_selected, top_k, sm_scale, out, lse): the same
  * metadata update, the same selection (written to selected / n_selected, and
- * the scores to `scores` when it is not NULL), the same outputs.  Two
- * launches: the scoring grid (with the refresh), then the decode, whose CTAs
- * rank their own rows first when the rows go one row per k CTAs (see
- * qskv_sparse_paged_decode); otherwise the ranking kernel runs in between.
+ * the scores to `scores` when it is not NULL), the same outputs, bit for bit.
+ * Launches, by shape (rows = batch x num_kv_heads, k = decode CTAs per row as
+ * in qskv_sparse_paged_decode):
+ *   - k >= 2 and ceil(max_pages / k) pages of metadata fit a decode CTA's
+ *     staging memory (368 pages for head_dim 64, 176 for 128): one launch.
+ *     The k CTAs of a row form one thread-block cluster; the last one
+ *     refreshes the last page's metadata, each scores its share of the
+ *     row's pages, and after a cluster barrier each ranks the whole row and
+ *     decodes its share of the selected pages;
+ *   - otherwise k >= 1: the scoring grid (with the refresh), then the decode,
+ *     whose CTAs rank their own rows first: two launches;
+ *   - otherwise (more rows than fit one wave): scoring, ranking, decode.
  * bf16 KV only (QSKV_ERR_UNSUPPORTED otherwise); q fp32 or bf16; exact top-K
  * with the bound score.  Workspace: qskv_workspace_size(shape).  Same
  * argument checks and device errors as the two calls.

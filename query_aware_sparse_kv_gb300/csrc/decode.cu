@@ -92,10 +92,10 @@ __device__ __forceinline__ int unit_code(const DecodeArgs &a, int row, int slot,
 }
 
 // Code of logical page j of row `row` (a selected index the caller did not
-// pass: the fused rank + decode), with unit_code's checks.
-__device__ __forceinline__ int page_code(const DecodeArgs &a, int row, int j, const int32_t *pt_row) {
+// pass: the fused rank + decode), with unit_code's checks; seq: the row's
+// sequence length as read from seq_lens.
+__device__ __forceinline__ int page_code(const DecodeArgs &a, int row, int j, const int32_t *pt_row, int seq) {
     const int b = row / a.num_kv_heads;
-    int seq = __ldg(a.seq_lens + b);
     const int cap = a.max_pages * a.page_size;
     seq = seq < 0 ? 0 : (seq > cap ? cap : seq);  // flagged by the scoring kernel
     const int n_b = (seq + a.page_size - 1) / a.page_size;
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
             fence_proxy_async_smem();  // the keys' stores, before TMA refills of the same memory
             __syncthreads();
             for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
-                s_code[i] = i < nsel ? page_code(a, rc_row, s_code[i], a.pt_in_smem ? s_pt : nullptr) : -1;
+                s_code[i] = i < nsel ? page_code(a, rc_row, s_code[i], a.pt_in_smem ? s_pt : nullptr, rc_seq) : -1;
         } else {
             for (int i = threadIdx.x; i < a.slots_per_row; i += WPC * 32)
                 s_code[i] = unit_code(a, rc_row, i, a.pt_in_smem ? s_pt : nullptr);
