@@ -176,3 +176,68 @@ def test_select_decode_needs_bf16_kv():
                         dec.selected, dec.n_selected, dec.out, dec.shape, dec.workspace, lse=dec.lse)
     assert e.value.status == 2
     np.testing.assert_equal(dec.can_refresh_in_select, False)  # the engine takes the separate calls there
+
+
+@pytest.mark.parametrize("kind", ["gpt2_k2", "long_k8"])
+def test_one_launch_step_flags_device_index_errors(oracle_lib, kind):
+    """The one-launch step (the decode CTAs of a row score it): an out-of-pool
+    page id and an out-of-range sequence length are flagged
+    (QSKV_ERR_DEVICE_INDEX), skipped, and the call stays usable; after the
+    table is repaired the next step matches the oracle again."""
+    spec = _case(kind)
+    inp = W.make_inputs(spec)
+    dec = qskv.from_inputs(inp)
+    ids, vt = oracle_lib.all_pages(inp)
+    dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    dec.check()
+    n_pool = inp["k_pool"].shape[0]
+    good = dec.page_table[0, 3].item()
+    dec.page_table[0, 3] = n_pool + 5
+    dec.step(refresh_last=True)
+    with pytest.raises(qskv.QskvError) as e:
+        dec.check()
+    assert e.value.status == 5
+    assert torch.isfinite(dec.out).all()
+    dec.page_table[0, 3] = good
+    seq0 = dec.seq_lens[1].item()
+    dec.seq_lens[1] = dec.page_table.shape[1] * spec.page_size + 1  # beyond the table row
+    dec.step(refresh_last=True)
+    with pytest.raises(qskv.QskvError) as e:
+        dec.check()
+    assert e.value.status == 5
+    dec.seq_lens[1] = seq0
+    dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    dec.step(refresh_last=True)
+    dec.check()
+    torch.cuda.synchronize()
+    PR.check_rows(inp, dec, PR.sample_rows(spec.batch * spec.num_kv_heads, 12, seed=3), oracle_lib,
+                  oracle_meta=oracle_lib.meta(inp["k_pool"], ids, vt))
+
+
+def test_one_launch_step_in_a_cuda_graph(oracle_lib):
+    """The clustered one-launch step captured in a CUDA graph replays to the
+    same bits as the eager call."""
+    spec = _case("gpt2_k2")
+    inp = W.make_inputs(spec)
+    dec = qskv.from_inputs(inp)
+    ids, vt = oracle_lib.all_pages(inp)
+    dec.build_meta(torch.from_numpy(ids).cuda(), torch.from_numpy(vt).cuda())
+    dec.step(refresh_last=True)
+    dec.check()
+    torch.cuda.synchronize()
+    ref = (dec.out.clone(), dec.lse.clone(), dec.selected.clone())
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dec.step(refresh_last=True)
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(g):
+        dec.step(refresh_last=True)
+    for _ in range(2):
+        dec.out.fill_(float("nan"))
+        dec.selected.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        dec.check()
+        assert torch.equal(dec.out, ref[0]) and torch.equal(dec.lse, ref[1]) and torch.equal(dec.selected, ref[2])
