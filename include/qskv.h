@@ -299,7 +299,8 @@ qskv_status qskv_sparse_paged_decode(const void *q, qskv_dtype q_dtype, const vo
  *     The k CTAs of a row form one thread-block cluster; the last one
  *     refreshes the last page's metadata, each scores its share of the
  *     row's pages, and after a cluster barrier each ranks the whole row and
- *     decodes its share of the selected pages;
+ *     decodes its share of the selected pages (on a device where no cluster
+ *     of k such CTAs fits, the two-launch form below instead);
  *   - otherwise k >= 1: the scoring grid (with the refresh), then the decode,
  *     whose CTAs rank their own rows first: two launches;
  *   - otherwise (more rows than fit one wave): scoring, ranking, decode.

@@ -254,7 +254,8 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // row's 16-page groups [blk ng / k, (blk + 1) ng / k).  `stage` (stage_bytes
 // of shared memory) takes the page ids and metadata rows of as many groups
 // at a time as fit (the host takes this path only when one round covers a
-// CTA's share): the ids first (one coalesced pass), then the rows by
+// CTA's share): the ids first (one coalesced pass, unless the table row is
+// already in shared memory), then the rows by
 // 16-byte copies through L2 (consecutive threads copy consecutive chunks of
 // a row; chunk c of slot s sits at c ^ (s & 7), so the eight rows one
 // fragment load touches fall in different banks); each warp then scores
@@ -264,7 +265,7 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // copies (which are plain loads into shared memory, ordered by it).
 template <int D, bool QF32, int WPC>
 __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, int seq, int n_b, uint8_t *stage,
-                                size_t stage_bytes, const int32_t *pt_row, const void *s_q) {
+                                size_t stage_bytes, const int32_t *pt_row, bool pt_in_smem, const void *s_q) {
     constexpr int NKP = BoundScanRegs<D>::NKP;
     constexpr int ROWB = 4 * D;        // bytes of one bf16 metadata row [m | M]
     constexpr int CPRW = ROWB / 16;    // its 16-byte chunks
@@ -308,13 +309,19 @@ __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, in
     for (int rg = g0; rg < g1; rg += cap_groups) {
         const int ngr = min(cap_groups, g1 - rg);
         const int j0 = rg * 16;
-        for (int sl = threadIdx.x; sl < ngr * 16; sl += NT) s_ids[sl] = j0 + sl < n_b ? pt_row[j0 + sl] : -1;
-        __syncthreads();
+        // the round's page ids: the staged table row itself, else a copy
+        const int32_t *ids = s_ids;
+        if (pt_in_smem) {
+            ids = pt_row + j0;
+        } else {
+            for (int sl = threadIdx.x; sl < ngr * 16; sl += NT) s_ids[sl] = j0 + sl < n_b ? pt_row[j0 + sl] : -1;
+            __syncthreads();
+        }
         for (int i = threadIdx.x; i < ngr * 16 * CPRW; i += NT) {
             const int sl = i / CPRW, c = i % CPRW;
             const int j = j0 + sl;
             if (j < n_b) {
-                const int p = s_ids[sl];
+                const int p = ids[sl];
                 if (p >= 0 && p < a.num_pool_pages)
                     cp_async_cg16(stage + sl * ROWB + ((c ^ (sl & 7)) << 4),
                                   meta + (int64_t(p) * a.num_kv_heads + g) * ROWB + c * 16);
@@ -326,7 +333,7 @@ __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, in
             const int sa_ = gi * 16 + gid, sb_ = sa_ + 8;  // both = gid (mod 8)
             const int ja = j0 + sa_, jb = j0 + sb_;
             const bool va = ja < n_b, vb = jb < n_b;
-            const int pa = va ? s_ids[sa_] : 0, pb = vb ? s_ids[sb_] : 0;
+            const int pa = va ? ids[sa_] : 0, pb = vb ? ids[sb_] : 0;
             const bool bada = va && (pa < 0 || pa >= a.num_pool_pages);
             const bool badb = vb && (pb < 0 || pb >= a.num_pool_pages);
             if ((bada || badb) && t == 0) raise_error(a.flags, kErrPageId);
@@ -345,7 +352,9 @@ __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, in
                 if (vb) srow[jb] = badb ? NEG : sb;
             }
         }
-        __syncthreads();  // the stage is read, before the next round (or the ranking) reuses it
+        // the stage is read before the next round reuses it (after the last
+        // round, the caller's CTA or cluster barrier comes first)
+        if (rg + cap_groups < g1) __syncthreads();
     }
 }
 
@@ -454,7 +463,8 @@ __global__ void __launch_bounds__(WPC * 32, kDecodeCtasPerSm)
                 // the CTA's share of the row's scores, staged through the
                 // rings' memory; then every CTA of the row (cluster) sees all
                 score_row_share<D, QF32, WPC>(a, rc_row, rc_blk, rc_k, seq, n_b, ring0, size_t(WPC) * S * STAGE,
-                                              a.pt_in_smem ? s_pt : a.page_table + int64_t(b) * a.max_pages, s_q);
+                                              a.pt_in_smem ? s_pt : a.page_table + int64_t(b) * a.max_pages,
+                                              a.pt_in_smem != 0, s_q);
                 if (rc_k > 1)
                     cluster_sync();
                 else
@@ -1107,6 +1117,33 @@ cudaError_t launch_bf16_hint(const DecodeArgs &a, const CUtensorMap *tk, const C
     // the fused scoring shares a row's scores among its k CTAs: one cluster
     const unsigned cluster = SCORE && ROWCTA ? unsigned(a.row_blocks) : 1u;
     if (cluster > unsigned(kRowBlocksMax)) return cudaErrorInvalidConfiguration;
+    if (cluster > 1) {
+        // whether one cluster of these CTAs fits an SM group of this device
+        // (cached per device and cluster size for the last smem size asked)
+        static size_t fit_smem[64][kRowBlocksMax + 1] = {};
+        static int fit[64][kRowBlocksMax + 1] = {};
+        if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+        std::lock_guard<std::mutex> lock(mu);
+        if (fit_smem[dev][cluster] != smem) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cluster);
+            cfg.blockDim = dim3(WPC * 32);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            if (e != cudaSuccess) (void)cudaGetLastError();  // an answer of "no": not an error of the call
+            fit[dev][cluster] = e == cudaSuccess && n >= 1 ? 1 : 0;
+            fit_smem[dev][cluster] = smem;
+        }
+        if (!fit[dev][cluster]) return cudaErrorNotSupported;
+    }
     return launch_pdl_cluster(kernel, dim3(ctas), dim3(WPC * 32), smem, stream, cluster, *tk, *tv, a);
 }
 

@@ -529,10 +529,6 @@ qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_
     sa.seed = 0;
     sa.meta_evict_first = 0;
     sa.head_quads = 0;
-    if (!fused_score)
-        QSKV_TRY(launched(launch_page_select(sa, q_dtype, QSKV_BF16, shape->head_dim, st, scores != nullptr, 1,
-                                             fused ? 0 : 1),
-                          "select_decode scoring launch"));
 
     DecodeArgs a;
     a.q = q;
@@ -573,15 +569,23 @@ qskv_status qskv_select_decode(const void *q, qskv_dtype q_dtype, const void *k_
         a.selected_out = selected;
         a.n_selected_out = n_selected;
     }
-    if (fused_score) {
-        a.meta = meta;
-        a.meta_w = meta;
-        a.refresh = 1;
-        a.score_all = scores != nullptr ? 1 : 0;
-    }
     CUtensorMap tk, tv;
     QSKV_TRY(make_pool_map(&tk, k_pool, shape));
     QSKV_TRY(make_pool_map(&tv, v_pool, shape));
+    if (fused_score) {
+        DecodeArgs af = a;
+        af.meta = meta;
+        af.meta_w = meta;
+        af.refresh = 1;
+        af.score_all = scores != nullptr ? 1 : 0;
+        const cudaError_t e = launch_decode(af, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, st);
+        // cudaErrorNotSupported: no cluster of rk such CTAs fits this device
+        // (nothing was launched); the two-launch form below serves instead
+        if (e != cudaErrorNotSupported) return launched(e, "select_decode launch");
+    }
+    QSKV_TRY(launched(launch_page_select(sa, q_dtype, QSKV_BF16, shape->head_dim, st, scores != nullptr, 1,
+                                         fused ? 0 : 1),
+                      "select_decode scoring launch"));
     return launched(launch_decode(a, &tk, &tv, q_dtype, kv_dtype, shape->head_dim, grid, st),
                     "select_decode decode launch");
 }
