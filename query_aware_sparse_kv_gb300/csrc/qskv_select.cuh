@@ -379,8 +379,10 @@ __device__ int select_row(const SelectArgs &a, int row, int n_b, const float *sr
             eb += __popc(be);
         }
     } else {
+        // thread t walks the keys [t per, (t + 1) per); an odd run length
+        // puts the 32 lanes' reads of one step in 32 different banks
         const uint32_t thr = shr32(prefix, lo);
-        const int per = (n_b + NT - 1) / NT;
+        const int per = ((n_b + NT - 1) / NT) | 1;
         const int i0 = min(tid * per, n_b), i1 = min(i0 + per, n_b);
         int cg = 0, ce = 0;
         for (int i = i0; i < i1; i++) {
