@@ -701,7 +701,7 @@ class Bench:
 
 
 def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bound", approx: bool = False,
-                     one_call: bool = True) -> int:
+                     one_call: bool = True, sms: int | None = None) -> int:
     """The library's launches in one step: metadata refresh (inside the
     scoring launch for the exact bound top-K on bf16 KV), scoring, ranking
     (sparse only; inside the decode launch when the step is one call and the
@@ -714,7 +714,8 @@ def kernels_per_step(spec: W.Spec, inputs: dict, prefix: int, scorer: str = "bou
     CTA) or a row's stream-K pieces fit one warp's single round of loads
     (pieces x G x d / 128 <= 16, with the grid's 2 CTAs x 6 warps per SM); a
     cascade adds the prefix kernel."""
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if sms is None:
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     rows = spec.batch * spec.num_kv_heads
     spr = spec.top_k if spec.top_k is not None else inputs["page_table"].shape[1] - prefix
     upw = max(1, -(-rows * spr // (2 * sms * 6)))

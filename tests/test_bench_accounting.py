@@ -118,3 +118,24 @@ def test_source_hash_ignores_comments(tmp_path):
     b.write_text("// another comment\nint f() { return 1; }\n\n")
     c.write_text("int f() { return 2; }\n")
     assert bench.source_hash([a]) == bench.source_hash([b]) != bench.source_hash([c])
+
+
+def test_launches_per_step_of_each_workload():
+    """The bench line's gpu_launches claim, per step on a 152-SM GB300: one
+    launch for the GPT2-like step (its rows fit one wave split 2 ways, and a
+    CTA's 256 pages of metadata one staging round), two for the Llama-like
+    (k = 1) and long-context (512 pages per CTA: too many for one round)
+    steps, two for the cascade, five for the fp32 tiny batch; the separate
+    calls take three for the bf16 sparse steps."""
+    import torch
+
+    want = {"llama3_8b": 2, "gpt2_345m": 1, "long_context": 2, "shared_prefix": 2, "tiny": 5}
+    for name, n in want.items():
+        spec = W.spec_for(name)
+        pages = spec.max_pages or (spec.prefix_pages + spec.suffix_pages if spec.kind == "shared_prefix"
+                                   else -(-max(spec.seq_lens) // spec.page_size))
+        inputs = {"page_table": torch.empty((spec.batch, pages), dtype=torch.int32)}
+        prefix = spec.prefix_pages if spec.kind == "shared_prefix" else 0
+        assert bench.kernels_per_step(spec, inputs, prefix, sms=152) == n, name
+        if spec.top_k is not None and spec.kv_dtype == torch.bfloat16:
+            assert bench.kernels_per_step(spec, inputs, prefix, one_call=False, sms=152) == 3, name
