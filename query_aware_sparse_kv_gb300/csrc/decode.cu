@@ -261,8 +261,9 @@ __device__ void fold_shared_rows(const DecodeArgs &a, int row_first, int row_las
 // fragment load touches fall in different banks); each warp then scores
 // whole groups with bound_group_scores (the scoring kernel's product, in the
 // same order: equal bits) and stores them to the row's scores.  The last
-// page's new metadata is written before the CTA barrier that precedes the
-// copies (which are plain loads into shared memory, ordered by it).
+// page's metadata is recomputed by warp 0 of the CTA holding it while the
+// other pages' copies are in flight, and written both to meta and straight
+// into its staging slot (not copied).
 template <int D, bool QF32, int WPC>
 __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, int seq, int n_b, uint8_t *stage,
                                 size_t stage_bytes, const int32_t *pt_row, bool pt_in_smem, const void *s_q) {
@@ -277,15 +278,16 @@ __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, in
     const int ng = (n_b + 15) >> 4;
     const int g0 = int(int64_t(blk) * ng / k), g1 = int(int64_t(blk + 1) * ng / k);
     const char *meta = static_cast<const char *>(a.meta);
-    const int fresh_j = a.refresh && n_b > 0 ? n_b - 1 : -1;
-    if (fresh_j >= 0 && blk == k - 1 && warp == 0) {  // the CTA holding the last group
-        const int p = pt_row[fresh_j];
-        if (p >= 0 && p < a.num_pool_pages)  // a bad id is flagged by the scan below
-            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, p, g, seq - fresh_j * a.page_size, a.num_kv_heads,
-                                            a.page_size);
+    // the last page (its metadata recomputed here: the CTA holding the last group)
+    const int fresh_j = a.refresh && n_b > 0 && blk == k - 1 ? n_b - 1 : -1;
+    const int fresh_p = fresh_j >= 0 ? pt_row[fresh_j] : -1;
+    const bool fresh_ok = fresh_p >= 0 && fresh_p < a.num_pool_pages;  // a bad id is flagged by the scan
+    if (!(a.top_k < n_b || a.score_all)) {  // CTA-uniform: every page is kept, no score asked for
+        if (fresh_ok && warp == 0)
+            meta_tile_warp<Bf16Ops, D * 2>(a.k_pool, a.meta_w, fresh_p, g, seq - fresh_j * a.page_size,
+                                            a.num_kv_heads, a.page_size);
+        return;
     }
-    if (!(a.top_k < n_b || a.score_all)) return;  // CTA-uniform: every page is kept, no score asked for
-    __syncthreads();  // the refreshed row, before another warp reads it
 
     uint32_t bh[NKP][4], bl[NKP][4];
     {
@@ -320,12 +322,17 @@ __device__ void score_row_share(const DecodeArgs &a, int row, int blk, int k, in
         for (int i = threadIdx.x; i < ngr * 16 * CPRW; i += NT) {
             const int sl = i / CPRW, c = i % CPRW;
             const int j = j0 + sl;
-            if (j < n_b) {
+            if (j < n_b && j != fresh_j) {
                 const int p = ids[sl];
                 if (p >= 0 && p < a.num_pool_pages)
                     cp_async_cg16(stage + sl * ROWB + ((c ^ (sl & 7)) << 4),
                                   meta + (int64_t(p) * a.num_kv_heads + g) * ROWB + c * 16);
             }
+        }
+        if (fresh_ok && warp == 0 && fresh_j >= j0 && fresh_j < j0 + ngr * 16) {
+            const int sl = fresh_j - j0;
+            meta_tile_warp<Bf16Ops, D * 2, true>(a.k_pool, a.meta_w, fresh_p, g, seq - fresh_j * a.page_size,
+                                                  a.num_kv_heads, a.page_size, stage + sl * ROWB, sl & 7);
         }
         cp_async_wait_all();
         __syncthreads();

@@ -447,9 +447,12 @@ __device__ __forceinline__ uint4 shfl_xor4(uint4 v, int m) {
 // vector column, lanes holding the same column combine by shuffles, and the
 // two rows are written as 16-byte vectors.  Min / max are exact, so any
 // evaluation order gives the same bits (up to the sign of zero).
-template <class Ops, int ROW_BYTES>
+// TO_SMEM: the two rows also go to srow in shared memory, 16-byte chunk c of
+// the [m | M] row at chunk position c ^ swz.
+template <class Ops, int ROW_BYTES, bool TO_SMEM = false>
 __device__ __forceinline__ void meta_tile_warp(const void *k_pool, void *meta, int p, int g, int valid,
-                                               int num_kv_heads, int page_size) {
+                                               int num_kv_heads, int page_size, uint8_t *srow = nullptr,
+                                               int swz = 0) {
     constexpr int CPR = ROW_BYTES / 16;  // 16-byte chunks per token row
     constexpr int RP = 32 / CPR;         // token rows read in parallel by one warp
     static_assert(CPR >= 1 && CPR <= 32 && 32 % CPR == 0, "row must be 16..512 bytes");
@@ -481,6 +484,10 @@ __device__ __forceinline__ void meta_tile_warp(const void *k_pool, void *meta, i
     uint8_t *out = static_cast<uint8_t *>(meta) + (int64_t(p) * num_kv_heads + g) * 2 * ROW_BYTES;
     if (r0 == 0) *reinterpret_cast<uint4 *>(out + c * 16) = mn;
     if (r0 == (RP > 1 ? 1 : 0)) *reinterpret_cast<uint4 *>(out + ROW_BYTES + c * 16) = mx;
+    if constexpr (TO_SMEM) {
+        if (r0 == 0) *reinterpret_cast<uint4 *>(srow + ((c ^ swz) << 4)) = mn;
+        if (r0 == (RP > 1 ? 1 : 0)) *reinterpret_cast<uint4 *>(srow + (((CPR + c) ^ swz) << 4)) = mx;
+    }
 }
 
 // ------------------------------------------------------- kernel arguments --
