@@ -174,8 +174,8 @@ def select_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, m
                   lse: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
                   stream=None):
     """One decode step: last-page metadata refresh, bound scores, exact top-K
-    and the sparse decode (two launches; the decode ranks its own rows when
-    they go one row per k CTAs)."""
+    and the sparse decode (one to three launches by shape, see
+    qskv_select_decode in include/qskv.h)."""
     _check(load().qskv_select_decode(_ptr(q), _dtype(q), _ptr(k_pool), _ptr(v_pool), _ptr(meta), _dtype(k_pool),
                                      _ptr(page_table), _ptr(seq_lens), ctypes.byref(shape), int(top_k),
                                      float(sm_scale), _ptr(selected), _ptr(n_selected), _ptr(scores), _ptr(out),

@@ -158,3 +158,25 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             binding.load(str(tmp_path / "missing.so"))
     finally:
         binding._lib = saved
+
+
+def test_select_decode_argument_checks(lib):
+    """The one-call step rejects what it cannot do before any launch."""
+    shape = qskv.make_shape(2, 8, 2, 128, 16, 8, 16)
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+
+    def call(q=p, kv_dtype=1, k_pool=p, top_k=4, scale=0.0, out=p, lse=None, shp=shape):
+        return lib.qskv_select_decode(q, 1, k_pool, p, p, kv_dtype, p, p, ctypes.byref(shp), top_k, scale, p, p, None,
+                                      out, lse, p, 4096, None)
+
+    assert call(kv_dtype=0) == 2                     # fp32 KV: the separate calls serve it
+    assert "bf16" in lib.qskv_last_error_message().decode()
+    assert call(k_pool=None) == 1                    # NULL K pool
+    assert call(top_k=0) == 1
+    assert call(scale=-1.0) == 1
+    assert call(out=ctypes.c_void_p(base + 4)) == 1  # misaligned output
+    assert call(lse=ctypes.c_void_p(base + 2)) == 1  # misaligned lse
+    assert call(q=ctypes.c_void_p(base + 8)) == 1    # misaligned query
+    assert call(shp=qskv.make_shape(2, 8, 2, 96, 16, 8, 16)) == 2  # head_dim 96
